@@ -1,0 +1,350 @@
+"""Pins for the CPU oracle: checks against facts fixed by the mathematics and
+by hand-derived fixtures, not against the oracle's own formulas.
+
+Each test names the mistake it is there to catch.  The pages print no
+worked example or value for this path, so the fixtures under tests/golden/
+are hand-derived and cite the passage they follow.
+"""
+
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_sparse_linear_scores_b300 import synth
+from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, Workload, frames_tensor
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def hexf(h: str) -> float:
+    return struct.unpack("<f", struct.pack("<I", int(h, 16)))[0]
+
+
+def bf16(x) -> torch.Tensor:
+    return torch.as_tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
+
+
+def rnd(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g, dtype=torch.float64) * scale).to(torch.float32).to(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------
+# pooling
+# --------------------------------------------------------------------------
+def test_pool_golden_order_and_division():
+    """Catches: pairwise/reversed summation; reciprocal multiply instead of divide."""
+    for line in open(os.path.join(GOLDEN, "pool_order.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        name, rest = line.split(None, 1)
+        toks, exp = rest.split("->")
+        vals = [hexf(t) for t in toks.split()]
+        x = bf16(np.array(vals, np.float32).reshape(1, len(vals), 1).repeat(4, axis=2))
+        assert torch.equal(x.float(), torch.tensor(vals).view(1, -1, 1).repeat(1, 1, 4)), "inputs must be bf16-exact"
+        out = oracle.pool(x, beta=len(vals))
+        assert out.shape == (1, 4)
+        assert np.all(out.view(np.uint32) == np.uint32(int(exp, 16))), (name, out)
+
+
+def test_pool_constant_blocks_exact():
+    """A block of identical tokens pools to that value exactly (full and partial blocks)."""
+    nf, d, beta = 10, 8, 4                   # blocks of 4, 4, 2 tokens per frame
+    c = np.linspace(-3, 3, d).astype(np.float32)
+    x = bf16(np.broadcast_to(c, (2, nf, d)))
+    out = oracle.pool(x, beta)
+    assert out.shape == (2 * 3, d)
+    np.testing.assert_array_equal(out, np.broadcast_to(x[0, 0].float().numpy(), out.shape))
+
+
+def test_pool_tiles_each_frame_separately():
+    """Catches flat tiling across frame boundaries: with N_f = 5 and beta = 2 the
+    blocks of every frame are tokens {0,1}, {2,3}, {4}."""
+    nf, beta = 5, 2
+    t = np.arange(nf, dtype=np.float32)
+    x = bf16(np.stack([t, t + 10]).reshape(2, nf, 1).repeat(4, axis=2))
+    out = oracle.pool(x, beta)[:, 0]
+    np.testing.assert_array_equal(out, [0.5, 2.5, 4.0, 10.5, 12.5, 14.0])
+
+
+# --------------------------------------------------------------------------
+# scores
+# --------------------------------------------------------------------------
+def test_scores_fused_multiply_add():
+    """Catches a separately rounded multiply then add: (1+2^-12)^2 - 1 is
+    2^-11 + 2^-24 with one rounding, 2^-11 with two."""
+    a = np.float32(1 + 2.0 ** -12)
+    qp = np.array([[-1.0, a]], np.float32)
+    kp = np.array([[1.0, a]], np.float32)
+    s = oracle.scores(qp, kp)
+    assert s[0, 0] == np.float32(2.0 ** -11 + 2.0 ** -24)
+
+
+def test_scores_channel_order():
+    """Catches a reversed or tree-shaped channel reduction: 1 + 1e8 - 1e8 is 0 in
+    ascending float order and 1 in descending order."""
+    qp = np.array([[1.0, 1e8, -1e8]], np.float32)
+    kp = np.ones((1, 3), np.float32)
+    assert oracle.scores(qp, kp)[0, 0] == 0.0
+    assert oracle.scores(qp[:, ::-1].copy(), kp)[0, 0] == 1.0
+
+
+def test_scores_orthogonal_and_unit_vectors():
+    """Catches a transposed score matrix or an index mix-up."""
+    d = 16
+    qp = np.eye(d, dtype=np.float32)[:3] * np.float32(2)
+    kp = np.arange(5 * d, dtype=np.float32).reshape(5, d)
+    s = oracle.scores(qp, kp)
+    assert s.shape == (3, 5)
+    np.testing.assert_array_equal(s, 2 * kp[:, :3].T)
+
+
+# --------------------------------------------------------------------------
+# top-K
+# --------------------------------------------------------------------------
+def _read_topk_golden():
+    rows, exp, k, mode = [], [], None, None
+    for line in open(os.path.join(GOLDEN, "topk_ties.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line in ("scores", "expected"):
+            mode = line
+            continue
+        if line.startswith("k "):
+            k = int(line.split()[1])
+            continue
+        (rows if mode == "scores" else exp).append([float(v) for v in line.split()])
+    return np.array(rows, np.float32), k, np.array(exp, np.int32)
+
+
+def test_topk_golden_ties():
+    """Catches: higher index winning a tie; output not in ascending index order;
+    -0 and +0 treated as different."""
+    s, k, exp = _read_topk_golden()
+    np.testing.assert_array_equal(oracle.topk(s, k), exp)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_brute_force(seed):
+    """Brute force on small random rows with many planted ties."""
+    rng = np.random.default_rng(seed)
+    nqb, nkb = 7, 13
+    s = rng.integers(-3, 4, size=(nqb, nkb)).astype(np.float32) * np.float32(0.5)
+    for k in (1, 4, nkb):
+        got = oracle.topk(s, k)
+        for r in range(nqb):
+            order = sorted(range(nkb), key=lambda i: (-float(s[r, i]), i))
+            assert list(got[r]) == sorted(order[:k])
+
+
+def test_topk_all_blocks_when_k_is_nkb():
+    s = np.random.default_rng(1).standard_normal((4, 9)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.topk(s, 9), np.tile(np.arange(9), (4, 1)))
+
+
+def test_topk_rejects_bad_k_and_nonfinite():
+    s = np.zeros((2, 5), np.float32)
+    with pytest.raises(ValueError):
+        oracle.topk(s, 0)
+    with pytest.raises(ValueError):
+        oracle.topk(s, 6)
+    s[1, 2] = np.nan
+    with pytest.raises(ValueError):
+        oracle.topk(s, 2)
+
+
+# --------------------------------------------------------------------------
+# attention: reductions to textbook cases
+# --------------------------------------------------------------------------
+def dense_window_attention(q, k, v, scale):
+    """Textbook softmax attention of every query over every key (float64)."""
+    q = q.double().numpy()
+    k = k.double().numpy()
+    v = v.double().numpy()
+    l = scale * q @ k.T
+    l -= l.max(axis=1, keepdims=True)
+    p = np.exp(l)
+    return (p @ v) / p.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("nf,beta,C,n_win,d", [(12, 4, 1, 3, 8), (10, 4, 2, 3, 16), (7, 3, 2, 2, 8)])
+def test_all_blocks_empty_state_is_dense_window_attention(nf, beta, C, n_win, d):
+    """K = all key blocks and an empty state give dense sliding-window softmax
+    attention.  Catches: a missing or wrong scale, a missing block, a mask
+    inside the window, a non-zero linear read of the empty state."""
+    BH = 2
+    Q = rnd((BH, C * nf, d), 1)
+    K = rnd((BH, n_win * nf, d), 2)
+    V = rnd((BH, n_win * nf, d), 3)
+    nkb = n_win * -(-nf // beta)
+    out = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=nkb)
+    for h in range(BH):
+        ref = dense_window_attention(Q[h], K[h], V[h], 1 / math.sqrt(d))
+        np.testing.assert_allclose(out["O"][h], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_one_selected_block_is_softmax_over_that_block():
+    """K = 1: each query attends to exactly the block its pooled score ranks
+    first (checked by brute force) and nothing else."""
+    nf, beta, C, n_win, d = 8, 4, 1, 3, 8
+    Q, K, V = rnd((1, C * nf, d), 4), rnd((1, n_win * nf, d), 5), rnd((1, n_win * nf, d), 6)
+    out = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=1)
+    qf, kf = Q[0].float().numpy(), K[0].float().numpy()
+    for qb in range(2):
+        qmean = qf[qb * beta:(qb + 1) * beta].mean(0)
+        kmeans = [kf[w * nf + j * beta: w * nf + (j + 1) * beta].mean(0) for w in range(n_win) for j in range(2)]
+        best = int(np.argmax([float(np.dot(qmean, km)) for km in kmeans]))
+        assert out["idx"][0, qb, 0] == best
+        w, j = divmod(best, 2)
+        sl = slice(w * nf + j * beta, w * nf + (j + 1) * beta)
+        ref = dense_window_attention(Q[0, qb * beta:(qb + 1) * beta], K[0, sl], V[0, sl], 1 / math.sqrt(d))
+        np.testing.assert_allclose(out["O"][0, qb * beta:(qb + 1) * beta], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_single_key_gives_its_value():
+    """One token per frame, one frame: softmax over one key is 1, o = v exactly."""
+    d = 8
+    Q, K, V = rnd((1, 1, d), 7), rnd((1, 1, d), 8), rnd((1, 1, d), 9)
+    out = oracle.hybrid_forward(Q, K, V, None, None, C=1, n_win=1, nf=1, beta=1, k=1)
+    np.testing.assert_array_equal(out["O"][0, 0], V[0, 0].double().numpy())
+
+
+def test_key_permutation_within_frame_invariance():
+    """K = all: permuting tokens inside a frame (same permutation for K and V)
+    leaves the output unchanged."""
+    nf, beta, C, n_win, d = 12, 4, 1, 3, 16
+    Q, K, V = rnd((1, C * nf, d), 10), rnd((1, n_win * nf, d), 11), rnd((1, n_win * nf, d), 12)
+    perm = torch.randperm(nf, generator=torch.Generator().manual_seed(0))
+    Kp, Vp = K.clone(), V.clone()
+    Kp[0, nf:2 * nf] = K[0, nf:2 * nf][perm]
+    Vp[0, nf:2 * nf] = V[0, nf:2 * nf][perm]
+    nkb = n_win * 3
+    a = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=nkb)["O"]
+    b = oracle.hybrid_forward(Q, Kp, Vp, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=nkb)["O"]
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# state, linear read, sum of the two paths
+# --------------------------------------------------------------------------
+def test_phi_and_single_token_state_closed_form():
+    """phi = elu + 1 at exact points; S = phi(k) v^T (not v phi(k)^T), z = phi(k)."""
+    kv = np.array([0.0, 1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 3.0], np.float32)
+    vv = np.arange(1, 9, dtype=np.float32)
+    S = np.zeros((8, 8))
+    z = np.zeros(8)
+    oracle.absorb(S, z, bf16(kv[None]), bf16(vv[None]))
+    phi = np.where(kv > 0, kv + 1.0, np.exp(kv.astype(np.float64)))
+    np.testing.assert_array_equal(phi[:4], [1.0, 2.0, math.exp(-1.0), 3.0])
+    np.testing.assert_allclose(z, phi, rtol=1e-15)
+    np.testing.assert_allclose(S, np.outer(phi, vv), rtol=1e-15)
+
+
+def test_incremental_absorb_equals_one_shot():
+    """Frame-by-frame absorption = absorbing every evicted frame at once."""
+    d, nf = 16, 6
+    Kev, Vev = rnd((1, 5 * nf, d), 13), rnd((1, 5 * nf, d), 14)
+    S1, z1 = oracle.state_from_frames(Kev, Vev)
+    S2, z2 = None, None
+    for f in range(5):
+        S2, z2 = oracle.state_from_frames(Kev[:, f * nf:(f + 1) * nf], Vev[:, f * nf:(f + 1) * nf], S2, z2)
+    np.testing.assert_allclose(S2, S1, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(z2, z1, rtol=1e-12)
+
+
+def test_linear_read_one_token_and_empty_state():
+    """One absorbed token: o = v * a/(a + eps) with a = phi(q).phi(k).
+    Empty state: o = 0 exactly."""
+    d = 8
+    q, k, v = rnd((3, d), 15), rnd((1, d), 16), rnd((1, d), 17)
+    S, z = np.zeros((d, d)), np.zeros(d)
+    assert np.all(oracle.linear_read(q, S, z) == 0.0)
+    oracle.absorb(S, z, k, v)
+    phi = lambda x: np.where(x > 0, x + 1, np.exp(np.minimum(x, 0)))
+    pq, pk = phi(q.double().numpy()), phi(k.double().numpy()[0])
+    a = pq @ pk
+    ref = (a / (a + 1e-6))[:, None] * v.double().numpy()[0][None, :]
+    np.testing.assert_allclose(oracle.linear_read(q, S, z), ref, rtol=1e-13)
+
+
+def test_constant_values_give_constant_output():
+    """V = c everywhere (window and evicted): empty state -> O = c;
+    with a state -> O = c * (1 + a/(a + eps)), a = phi(q).z, the same c in
+    every row.  Catches a missing normalisation in either path."""
+    nf, beta, C, n_win, d = 8, 4, 1, 2, 8
+    Q, K = rnd((1, C * nf, d), 18), rnd((1, n_win * nf, d), 19)
+    c = np.linspace(-1, 1, d).astype(np.float32)
+    V = bf16(np.broadcast_to(c, (1, n_win * nf, d)))
+    cv = V[0, 0].double().numpy()
+    out = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=2)
+    np.testing.assert_allclose(out["O"][0], np.broadcast_to(cv, (nf, d)), rtol=1e-14, atol=1e-15)
+    Kev = rnd((1, 3 * nf, d), 20)
+    Vev = bf16(np.broadcast_to(c, (1, 3 * nf, d)))
+    S, z = oracle.state_from_frames(Kev, Vev)
+    out = oracle.hybrid_forward(Q, K, V, S, z, C=C, n_win=n_win, nf=nf, beta=beta, k=2)
+    phi = lambda x: np.where(x > 0, x + 1, np.exp(np.minimum(x, 0)))
+    a = phi(Q[0].double().numpy()) @ z[0]
+    np.testing.assert_allclose(out["O"][0], cv[None, :] * (1 + a / (a + 1e-6))[:, None], rtol=1e-12)
+
+
+def test_output_is_sum_of_paths_and_rows_subset():
+    """O = O_swa + O_lin, O_lin equals the standalone linear read, and a row
+    subset reproduces the same rows."""
+    w = CONFIGS["tiny"]
+    s = 5
+    Q = frames_tensor(w, synth.STREAM_Q, w.chunk(s)).reshape(w.heads_total, -1, w.head_dim)
+    K = frames_tensor(w, synth.STREAM_K, w.window(s)).reshape(w.heads_total, -1, w.head_dim)
+    V = frames_tensor(w, synth.STREAM_V, w.window(s)).reshape(w.heads_total, -1, w.head_dim)
+    ev = list(range(w.absorbed_before(s)))
+    S, z = oracle.state_from_frames(frames_tensor(w, synth.STREAM_K, ev).reshape(w.heads_total, -1, w.head_dim),
+                                    frames_tensor(w, synth.STREAM_V, ev).reshape(w.heads_total, -1, w.head_dim))
+    kw = dict(C=w.chunk_frames, n_win=w.n_win(s), nf=w.tokens_per_frame, beta=w.block_size, k=w.k_for(s))
+    full = oracle.hybrid_forward(Q, K, V, S, z, split=True, **kw)
+    np.testing.assert_allclose(full["O"], full["O_swa"] + full["O_lin"], rtol=1e-15, atol=0)
+    for h in range(w.heads_total):
+        np.testing.assert_allclose(full["O_lin"][h], oracle.linear_read(Q[h], S[h], z[h]), rtol=1e-14)
+    rows = [0, 5, 31, 64, 127]
+    sub = oracle.hybrid_forward(Q, K, V, S, z, rows=rows, **kw)
+    np.testing.assert_array_equal(sub["O"], full["O"][:, rows])
+    np.testing.assert_array_equal(sub["idx"], full["idx"])
+
+
+def test_selection_changes_with_k_only_by_inclusion():
+    """The K-block selection is nested: raising K only adds blocks."""
+    w = CONFIGS["tiny"]
+    Q = frames_tensor(w, synth.STREAM_Q, [5])[0]
+    K = frames_tensor(w, synth.STREAM_K, [4, 5])[0]
+    s = oracle.scores(oracle.pool(Q, 32), oracle.pool(K, 32))
+    prev = None
+    for k in range(1, 9):
+        cur = oracle.topk(s, k)
+        if prev is not None:
+            for r in range(cur.shape[0]):
+                assert set(prev[r]) <= set(cur[r])
+        prev = cur
+
+
+def test_generator_known_answers():
+    """Philox4x32-10 known-answer vectors (Random123 distribution) pin the
+    input generator, so the same inputs can be rebuilt anywhere."""
+    z = lambda v: torch.tensor([v], dtype=torch.int64)
+    out = synth.philox4x32_10(z(0), z(0), z(0), z(0), 0, 0)
+    assert [int(x) for x in out] == [0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8]
+    M = 0xFFFFFFFF
+    out = synth.philox4x32_10(z(M), z(M), z(M), z(M), M, M)
+    assert [int(x) for x in out] == [0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD]
+
+
+def test_generator_moments_and_frame_independence():
+    w = CONFIGS["tiny"]
+    a = frames_tensor(w, synth.STREAM_K, [0, 1, 2])
+    b = frames_tensor(w, synth.STREAM_K, [2])
+    assert torch.equal(a[:, 2:3], b)
+    x = a.double()
+    assert abs(float(x.mean())) < 0.02 and abs(float(x.std()) - 1.0) < 0.02
