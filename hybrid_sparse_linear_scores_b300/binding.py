@@ -1,0 +1,186 @@
+"""ctypes binding of libhf.so (include/hf.h), same names as the C entry points.
+
+Argument marshalling only: tensors are passed as raw device pointers, every
+step runs in the library's CUDA kernels.  There is no fallback: if libhf.so
+is missing or a call fails, an exception is raised.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libhf.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "hf.h")
+
+HF_OK = 0
+STATUS = {0: "HF_OK", 1: "HF_ERR_INVALID_ARG", 2: "HF_ERR_UNSUPPORTED", 3: "HF_ERR_CUDA",
+          4: "HF_ERR_TIMEOUT", 5: "HF_ERR_DEVICE_CHECK"}
+
+
+class HFError(RuntimeError):
+    def __init__(self, code: int, func: str, detail: str):
+        self.code = code
+        super().__init__(f"{func}: {STATUS.get(code, code)}: {detail}")
+
+
+class HFConfig(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("tokens_per_frame", ctypes.c_int32), ("window_frames", ctypes.c_int32),
+                ("chunk_frames", ctypes.c_int32), ("block_size", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("lin_eps", ctypes.c_float)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not found: build it with "
+                               "`python -m hybrid_sparse_linear_scores_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        cfgp = ctypes.POINTER(HFConfig)
+        sig = {
+            "hf_abi_version": ([], _I),
+            "hf_status_string": ([_I], ctypes.c_char_p),
+            "hf_last_error": ([], ctypes.c_char_p),
+            "hf_workspace_size": ([cfgp, ctypes.POINTER(ctypes.c_size_t)], _I),
+            "hf_state_reset": ([cfgp, _P, _P, _P], _I),
+            "hf_absorb_evicted": ([cfgp, _P, _P, _P, _P, _I, _P, _P], _I),
+            "hf_absorb_evicted_strided": ([cfgp, _P, _P, _P, _P, _I, ctypes.c_int64, _P, _P], _I),
+            "hf_block_scores": ([cfgp, _P, _P, _I, _P, _I, _P, _P, _P], _I),
+            "hf_topk_blocks": ([cfgp, _P, _I, _I, _P, _P], _I),
+            "hf_sparse_swa_attn": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P], _I),
+            "hf_linear_read": ([cfgp, _P, _P, _P, _P, _I, _P], _I),
+            "hf_hybrid_forward": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P], _I),
+            "hf_hybrid_forward_profiled": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P,
+                                            ctypes.POINTER(ctypes.c_void_p)], _I),
+            "hf_get_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
+            "hf_selftest_wait_timeout": ([_P, _I, _P], _I),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/hf.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^HF_API\s+(?:const\s+)?[a-z_0-9]+\s*\*?\s*(hf_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def make_config(batch, heads, head_dim, tokens_per_frame, window_frames, chunk_frames, block_size, topk,
+                softmax_scale=0.0, lin_eps=1e-6) -> HFConfig:
+    return HFConfig(batch, heads, head_dim, tokens_per_frame, window_frames, chunk_frames, block_size, topk,
+                    softmax_scale, lin_eps)
+
+
+def _check(rc: int, name: str):
+    if rc != HF_OK:
+        raise HFError(rc, name, lib().hf_last_error().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _slots(slot_map):
+    if slot_map is None:
+        return None
+    arr = (ctypes.c_int32 * len(slot_map))(*[int(s) for s in slot_map])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def hf_workspace_size(cfg: HFConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().hf_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "hf_workspace_size")
+    return n.value
+
+
+def hf_state_reset(cfg, S, z, stream=None):
+    _check(lib().hf_state_reset(ctypes.byref(cfg), _ptr(S), _ptr(z), _stream(stream)), "hf_state_reset")
+
+
+def hf_absorb_evicted(cfg, S, z, K_ev, V_ev, n_ev_tokens, ws, stream=None):
+    _check(lib().hf_absorb_evicted(ctypes.byref(cfg), _ptr(S), _ptr(z), _ptr(K_ev), _ptr(V_ev), int(n_ev_tokens),
+                                   _ptr(ws), _stream(stream)), "hf_absorb_evicted")
+
+
+def hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, head_stride_tokens, ws, stream=None):
+    _check(lib().hf_absorb_evicted_strided(ctypes.byref(cfg), _ptr(S), _ptr(z), _ptr(K_ev), _ptr(V_ev),
+                                           int(n_ev_tokens), int(head_stride_tokens), _ptr(ws), _stream(stream)),
+           "hf_absorb_evicted_strided")
+
+
+def hf_block_scores(cfg, Q, Kc, slot_stride, slot_map, n_win, scores, ws, stream=None):
+    sm = _slots(slot_map)
+    _check(lib().hf_block_scores(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), int(slot_stride), sm and sm[0], int(n_win),
+                                 _ptr(scores), _ptr(ws), _stream(stream)), "hf_block_scores")
+
+
+def hf_topk_blocks(cfg, scores, nQB, nKB, idx, stream=None):
+    _check(lib().hf_topk_blocks(ctypes.byref(cfg), _ptr(scores), int(nQB), int(nKB), _ptr(idx), _stream(stream)),
+           "hf_topk_blocks")
+
+
+def hf_sparse_swa_attn(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, idx, O_swa, ws, stream=None):
+    sm = _slots(slot_map)
+    _check(lib().hf_sparse_swa_attn(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride), sm and sm[0],
+                                    int(n_win), _ptr(idx), _ptr(O_swa), _ptr(ws), _stream(stream)),
+           "hf_sparse_swa_attn")
+
+
+def hf_linear_read(cfg, Q, S, z, O, accumulate=False, stream=None):
+    _check(lib().hf_linear_read(ctypes.byref(cfg), _ptr(Q), _ptr(S), _ptr(z), _ptr(O), int(bool(accumulate)),
+                                _stream(stream)), "hf_linear_read")
+
+
+def hf_hybrid_forward(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream=None):
+    sm = _slots(slot_map)
+    _check(lib().hf_hybrid_forward(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride), sm and sm[0],
+                                   int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out), _ptr(ws), _stream(stream)),
+           "hf_hybrid_forward")
+
+
+def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, events,
+                               stream=None):
+    """events: 5 torch.cuda.Event objects (recorded between the kernels)."""
+    sm = _slots(slot_map)
+    ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
+    _check(lib().hf_hybrid_forward_profiled(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
+                                            sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
+                                            _ptr(ws), _stream(stream), ev), "hf_hybrid_forward_profiled")
+
+
+def hf_get_device_status(ws, stream=None) -> tuple[int, int]:
+    """(status code, site) of the first device-side error since the last call."""
+    site = ctypes.c_int32(0)
+    rc = lib().hf_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(site))
+    return rc, site.value
+
+
+def hf_selftest_wait_timeout(ws, limit_us, stream=None):
+    _check(lib().hf_selftest_wait_timeout(_ptr(ws), int(limit_us), _stream(stream)), "hf_selftest_wait_timeout")

@@ -1,0 +1,405 @@
+// hf_api.cu -- the C ABI declared in include/hf.h: argument validation,
+// workspace layout, tensor-map encoding and the launch sequence of each
+// entry point.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "hf.h"
+#include "hf_internal.h"
+
+namespace hf {
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+hf_status fail(hf_status s, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+hf_status cuda_fail(int err, const char* what)
+{
+    return fail(HF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(static_cast<cudaError_t>(err)));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align1k(size_t x) { return (x + 1023) & ~size_t(1023); }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// ---- config ---------------------------------------------------------------
+hf_status check_cfg(const hf_config* cfg)
+{
+    if (!cfg) return fail(HF_ERR_INVALID_ARG, "cfg is NULL");
+    if (cfg->batch < 1 || cfg->heads < 1) return fail(HF_ERR_INVALID_ARG, "batch and heads must be >= 1");
+    if (cfg->head_dim != 64 && cfg->head_dim != 128)
+        return fail(HF_ERR_UNSUPPORTED, "head_dim %d not in {64, 128}", cfg->head_dim);
+    if (cfg->tokens_per_frame < 1) return fail(HF_ERR_INVALID_ARG, "tokens_per_frame must be >= 1");
+    if (cfg->window_frames < 1 || cfg->window_frames > HF_MAX_WINDOW_FRAMES)
+        return fail(HF_ERR_UNSUPPORTED, "window_frames %d not in [1, %d]", cfg->window_frames, HF_MAX_WINDOW_FRAMES);
+    if (cfg->chunk_frames < 1 || cfg->chunk_frames > cfg->window_frames)
+        return fail(HF_ERR_INVALID_ARG, "chunk_frames %d not in [1, window_frames]", cfg->chunk_frames);
+    if (cfg->block_size != 32 && cfg->block_size != 64 && cfg->block_size != 128)
+        return fail(HF_ERR_UNSUPPORTED, "block_size %d not in {32, 64, 128}", cfg->block_size);
+    if (cfg->topk < 1) return fail(HF_ERR_INVALID_ARG, "topk must be >= 1");
+    if (!(cfg->softmax_scale >= 0.0f) || !std::isfinite(cfg->softmax_scale))
+        return fail(HF_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    if (!(cfg->lin_eps >= 0.0f) || !std::isfinite(cfg->lin_eps))
+        return fail(HF_ERR_INVALID_ARG, "lin_eps must be finite and >= 0");
+    const long bpf = ceil_div(cfg->tokens_per_frame, cfg->block_size);
+    if (bpf * cfg->window_frames > HF_MAX_KEY_BLOCKS)
+        return fail(HF_ERR_UNSUPPORTED, "window has %ld key blocks (> %d)", bpf * cfg->window_frames,
+                    HF_MAX_KEY_BLOCKS);
+    if ((long)cfg->batch * cfg->heads > (1L << 20)) return fail(HF_ERR_UNSUPPORTED, "batch*heads too large");
+    return HF_OK;
+}
+
+Geom make_geom(const hf_config* cfg, int n_win, int slot_stride)
+{
+    Geom g;
+    g.BH = cfg->batch * cfg->heads;
+    g.d = cfg->head_dim;
+    g.nf = cfg->tokens_per_frame;
+    g.C = cfg->chunk_frames;
+    g.W = cfg->window_frames;
+    g.n_win = n_win;
+    g.beta = cfg->block_size;
+    g.bpf = ceil_div(g.nf, g.beta);
+    g.nqb = g.C * g.bpf;
+    g.nkb = n_win * g.bpf;
+    g.k_eff = cfg->topk < g.nkb ? cfg->topk : g.nkb;
+    g.slot_stride = slot_stride;
+    const float scale = cfg->softmax_scale > 0.0f ? cfg->softmax_scale : 1.0f / std::sqrt((float)g.d);
+    g.scale_log2 = scale * 1.4426950408889634f;
+    g.eps = cfg->lin_eps;
+    return g;
+}
+
+WsLayout ws_layout(const hf_config* cfg)
+{
+    const size_t BH = (size_t)cfg->batch * cfg->heads;
+    const size_t d = (size_t)cfg->head_dim;
+    const size_t bpf = (size_t)ceil_div(cfg->tokens_per_frame, cfg->block_size);
+    const size_t nqb = (size_t)cfg->chunk_frames * bpf;
+    const size_t nkb = (size_t)cfg->window_frames * bpf;
+    const size_t kmax = (size_t)cfg->topk < nkb ? (size_t)cfg->topk : nkb;
+    WsLayout w;
+    w.status = 0;
+    w.qp = 1024;
+    w.kp = w.qp + align1k(BH * nqb * d * 4);
+    w.idx = w.kp + align1k(BH * nkb * d * 4);
+    w.smma = w.idx + align1k(BH * nqb * kmax * 4);
+    w.total = w.smma + align1k(BH * 2 * d * d * 2);
+    return w;
+}
+
+// ---- window arguments -------------------------------------------------------
+hf_status check_window(const hf_config* cfg, int32_t slot_stride, const int32_t* slot_map, int32_t n_win,
+                       SlotMap* sm)
+{
+    if (n_win < cfg->chunk_frames || n_win > cfg->window_frames)
+        return fail(HF_ERR_INVALID_ARG, "n_win %d not in [chunk_frames %d, window_frames %d]", n_win,
+                    cfg->chunk_frames, cfg->window_frames);
+    if (slot_stride < cfg->tokens_per_frame)
+        return fail(HF_ERR_INVALID_ARG, "slot_stride %d < tokens_per_frame %d", slot_stride, cfg->tokens_per_frame);
+    uint64_t used = 0;
+    for (int w = 0; w < HF_MAX_WINDOW_FRAMES; ++w) sm->s[w] = 0;
+    for (int w = 0; w < n_win; ++w) {
+        const int s = slot_map ? slot_map[w] : w;
+        if (s < 0 || s >= cfg->window_frames)
+            return fail(HF_ERR_INVALID_ARG, "slot_map[%d] = %d outside [0, %d)", w, s, cfg->window_frames);
+        if (used & (1ull << s)) return fail(HF_ERR_INVALID_ARG, "slot_map[%d] = %d used twice", w, s);
+        used |= 1ull << s;
+        sm->s[w] = s;
+    }
+    return HF_OK;
+}
+
+#define HF_CHECK_PTR(p)                                                                          \
+    do {                                                                                         \
+        if (!(p)) return fail(HF_ERR_INVALID_ARG, "%s is NULL", #p);                             \
+        if (!aligned16(p)) return fail(HF_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);     \
+    } while (0)
+
+#define HF_LAUNCH(expr, what)                                 \
+    do {                                                      \
+        const int e_ = (expr);                                \
+        if (e_ != 0) return cuda_fail(e_, what);              \
+    } while (0)
+
+// ---- tensor maps ------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+int make_tmap_bf16_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                      uint64_t stride2_bytes, uint32_t box0, uint32_t box1)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return (int)cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+}  // namespace hf
+
+using namespace hf;
+
+extern "C" {
+
+int32_t hf_abi_version(void) { return HF_ABI_VERSION; }
+
+const char* hf_status_string(hf_status s)
+{
+    switch (s) {
+    case HF_OK: return "HF_OK";
+    case HF_ERR_INVALID_ARG: return "HF_ERR_INVALID_ARG";
+    case HF_ERR_UNSUPPORTED: return "HF_ERR_UNSUPPORTED";
+    case HF_ERR_CUDA: return "HF_ERR_CUDA";
+    case HF_ERR_TIMEOUT: return "HF_ERR_TIMEOUT";
+    case HF_ERR_DEVICE_CHECK: return "HF_ERR_DEVICE_CHECK";
+    }
+    return "unknown hf_status";
+}
+
+const char* hf_last_error(void) { return g_last_error; }
+
+hf_status hf_workspace_size(const hf_config* cfg, size_t* bytes)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    if (!bytes) return fail(HF_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = ws_layout(cfg).total;
+    return HF_OK;
+}
+
+hf_status hf_state_reset(const hf_config* cfg, float* S, float* z, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(S);
+    HF_CHECK_PTR(z);
+    const Geom g = make_geom(cfg, cfg->chunk_frames, cfg->tokens_per_frame);
+    HF_LAUNCH(launch_state_reset(S, z, g, stream), "state reset launch");
+    return HF_OK;
+}
+
+hf_status hf_absorb_evicted_strided(const hf_config* cfg, float* S, float* z, const uint16_t* K_ev,
+                                    const uint16_t* V_ev, int32_t n_ev_tokens, int64_t head_stride_tokens, void* ws,
+                                    void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    if (n_ev_tokens < 0) return fail(HF_ERR_INVALID_ARG, "n_ev_tokens %d < 0", n_ev_tokens);
+    if (head_stride_tokens < n_ev_tokens)
+        return fail(HF_ERR_INVALID_ARG, "head_stride_tokens %lld < n_ev_tokens %d", (long long)head_stride_tokens,
+                    n_ev_tokens);
+    HF_CHECK_PTR(S);
+    HF_CHECK_PTR(z);
+    HF_CHECK_PTR(ws);
+    if (n_ev_tokens == 0) return HF_OK;
+    HF_CHECK_PTR(K_ev);
+    HF_CHECK_PTR(V_ev);
+    const Geom g = make_geom(cfg, cfg->chunk_frames, cfg->tokens_per_frame);
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + ws_layout(cfg).status);
+    HF_LAUNCH(launch_absorb(K_ev, V_ev, n_ev_tokens, head_stride_tokens, g, S, z, status, kDefaultWaitLimitNs, stream),
+              "absorb launch");
+    return HF_OK;
+}
+
+hf_status hf_absorb_evicted(const hf_config* cfg, float* S, float* z, const uint16_t* K_ev, const uint16_t* V_ev,
+                            int32_t n_ev_tokens, void* ws, void* stream)
+{
+    return hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, n_ev_tokens, ws, stream);
+}
+
+hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, int32_t slot_stride,
+                          const int32_t* slot_map, int32_t n_win, float* scores, void* ws, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(Q);
+    HF_CHECK_PTR(Kc);
+    HF_CHECK_PTR(scores);
+    HF_CHECK_PTR(ws);
+    SlotMap sm;
+    if ((s = check_window(cfg, slot_stride, slot_map, n_win, &sm)) != HF_OK) return s;
+    const Geom g = make_geom(cfg, n_win, slot_stride);
+    const WsLayout L = ws_layout(cfg);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* qp = reinterpret_cast<float*>(w + L.qp);
+    float* kp = reinterpret_cast<float*>(w + L.kp);
+    HF_LAUNCH(launch_pool(Q, Kc, g, sm, qp, kp, stream), "pool launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, scores, nullptr, stream), "score launch");
+    return HF_OK;
+}
+
+hf_status hf_topk_blocks(const hf_config* cfg, const float* scores, int32_t nQB, int32_t nKB, int32_t* idx,
+                         void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(scores);
+    HF_CHECK_PTR(idx);
+    if (nQB < 1 || nKB < 1) return fail(HF_ERR_INVALID_ARG, "nQB and nKB must be >= 1");
+    if (nKB > HF_MAX_KEY_BLOCKS) return fail(HF_ERR_UNSUPPORTED, "nKB %d > %d", nKB, HF_MAX_KEY_BLOCKS);
+    Geom g = make_geom(cfg, cfg->chunk_frames, cfg->tokens_per_frame);
+    g.nqb = nQB;
+    g.nkb = nKB;
+    g.k_eff = cfg->topk < nKB ? cfg->topk : nKB;
+    HF_LAUNCH(launch_topk(scores, g, idx, stream), "top-k launch");
+    return HF_OK;
+}
+
+hf_status hf_sparse_swa_attn(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                             int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const int32_t* idx,
+                             float* O_swa, void* ws, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(Q);
+    HF_CHECK_PTR(Kc);
+    HF_CHECK_PTR(Vc);
+    HF_CHECK_PTR(idx);
+    HF_CHECK_PTR(O_swa);
+    HF_CHECK_PTR(ws);
+    SlotMap sm;
+    if ((s = check_window(cfg, slot_stride, slot_map, n_win, &sm)) != HF_OK) return s;
+    const Geom g = make_geom(cfg, n_win, slot_stride);
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + ws_layout(cfg).status);
+    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, nullptr, nullptr, O_swa, nullptr, status, kDefaultWaitLimitNs,
+                          stream),
+              "sparse attention launch");
+    return HF_OK;
+}
+
+hf_status hf_linear_read(const hf_config* cfg, const uint16_t* Q, const float* S, const float* z, float* O,
+                         int32_t accumulate, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(Q);
+    HF_CHECK_PTR(S);
+    HF_CHECK_PTR(z);
+    HF_CHECK_PTR(O);
+    const Geom g = make_geom(cfg, cfg->chunk_frames, cfg->tokens_per_frame);
+    HF_LAUNCH(launch_linear_read(Q, S, z, g, O, accumulate, stream), "linear read launch");
+    return HF_OK;
+}
+
+hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                                     int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
+                                     const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream,
+                                     void* const* events)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(Q);
+    HF_CHECK_PTR(Kc);
+    HF_CHECK_PTR(Vc);
+    HF_CHECK_PTR(S);
+    HF_CHECK_PTR(z);
+    HF_CHECK_PTR(O);
+    HF_CHECK_PTR(ws);
+    if (idx_out && !aligned16(idx_out)) return fail(HF_ERR_INVALID_ARG, "idx_out is not 16-byte aligned");
+    SlotMap sm;
+    if ((s = check_window(cfg, slot_stride, slot_map, n_win, &sm)) != HF_OK) return s;
+    const Geom g = make_geom(cfg, n_win, slot_stride);
+    const WsLayout L = ws_layout(cfg);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    float* qp = reinterpret_cast<float*>(w + L.qp);
+    float* kp = reinterpret_cast<float*>(w + L.kp);
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + L.idx);
+    uint16_t* smma = reinterpret_cast<uint16_t*>(w + L.smma);
+    uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) -> int {
+        return events && events[i] ? (int)cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : 0;
+    };
+    HF_LAUNCH(mark(0), "event record");
+    HF_LAUNCH(launch_pool(Q, Kc, g, sm, qp, kp, stream), "pool launch");
+    HF_LAUNCH(mark(1), "event record");
+    HF_LAUNCH(launch_score_select(qp, kp, g, nullptr, idx, stream), "score/select launch");
+    HF_LAUNCH(mark(2), "event record");
+    HF_LAUNCH(launch_smma_prep(S, g, smma, stream), "state prep launch");
+    HF_LAUNCH(mark(3), "event record");
+    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, smma, z, nullptr, O, status, kDefaultWaitLimitNs, stream),
+              "hybrid attention launch");
+    HF_LAUNCH(mark(4), "event record");
+    return HF_OK;
+}
+
+hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                            int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
+                            const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream)
+{
+    return hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream,
+                                      nullptr);
+}
+
+hf_status hf_get_device_status(void* ws, void* stream, int32_t* site)
+{
+    if (!ws) return fail(HF_ERR_INVALID_ARG, "ws is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word[2] = {0, 0};
+    cudaError_t e = cudaMemcpyAsync(word, ws, sizeof word, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail((int)e, "status read");
+    if (word[0] != 0) {
+        const uint32_t zero[2] = {0, 0};
+        e = cudaMemcpyAsync(ws, zero, sizeof zero, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail((int)e, "status clear");
+    }
+    if (site) *site = (int32_t)word[1];
+    if (word[0] == 0) return HF_OK;
+    if (word[0] == HF_DEV_ERR_TIMEOUT)
+        return fail(HF_ERR_TIMEOUT, "device wait timed out at site %u", word[1]);
+    return fail(HF_ERR_DEVICE_CHECK, "device check failed at site %u (code %u)", word[1], word[0]);
+}
+
+hf_status hf_selftest_wait_timeout(void* ws, int32_t limit_us, void* stream)
+{
+    if (!ws) return fail(HF_ERR_INVALID_ARG, "ws is NULL");
+    if (limit_us < 1 || limit_us > 100000) return fail(HF_ERR_INVALID_ARG, "limit_us %d not in [1, 100000]", limit_us);
+    HF_LAUNCH(launch_selftest_wait(static_cast<uint32_t*>(ws), (uint64_t)limit_us * 1000ull, stream),
+              "self-test launch");
+    return HF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// hf_internal.h -- definitions shared by the library's .cu files (never by
+// the oracle): device error codes, derived geometry, kernel parameter blocks,
+// workspace layout and the launch functions each .cu file provides.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "hf.h"
+
+namespace hf {
+
+// Device status word codes (match hf_status values).
+constexpr uint32_t HF_DEV_ERR_TIMEOUT = 4;
+constexpr uint32_t HF_DEV_ERR_CHECK = 5;
+
+// Wait / check sites reported with a device error.
+enum Site : uint32_t {
+    SITE_ATTN_Q = 101,
+    SITE_ATTN_KV_FULL = 102,
+    SITE_ATTN_KV_EMPTY = 103,
+    SITE_ATTN_S_FULL = 104,
+    SITE_ATTN_P_FULL = 105,
+    SITE_ATTN_PV_DONE = 106,
+    SITE_ATTN_LIN = 107,
+    SITE_ATTN_PHIQ = 108,
+    SITE_ATTN_DRAIN = 109,
+    SITE_ATTN_BAD_INDEX = 110,
+    SITE_ABSORB_FULL = 201,
+    SITE_ABSORB_EMPTY = 202,
+    SITE_ABSORB_PHI = 203,
+    SITE_ABSORB_ACC = 204,
+    SITE_ABSORB_DRAIN = 205,
+    SITE_SELFTEST = 301,
+};
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s
+
+struct SlotMap {
+    int32_t s[HF_MAX_WINDOW_FRAMES];
+};
+
+// Geometry of one call, derived and validated on the host.
+struct Geom {
+    int32_t BH;          // batch * heads
+    int32_t d;           // head_dim
+    int32_t nf;          // tokens per frame
+    int32_t C;           // chunk frames
+    int32_t W;           // ring slots
+    int32_t n_win;       // frames in the window now
+    int32_t beta;        // block size
+    int32_t bpf;         // blocks per frame
+    int32_t nqb;         // query blocks (C * bpf)
+    int32_t nkb;         // key blocks (n_win * bpf)
+    int32_t k_eff;       // min(topk, nkb)
+    int32_t slot_stride; // rows per ring slot
+    float scale_log2;    // softmax scale * log2(e)
+    float eps;           // linear-read epsilon
+};
+
+// Workspace layout (byte offsets, 1024-aligned).
+struct WsLayout {
+    size_t status;   // 256 B: uint32 [0] code, [1] site
+    size_t qp;       // fp32 [BH][nQB][d]
+    size_t kp;       // fp32 [BH][nKB_max][d]
+    size_t idx;      // int32 [BH][nQB][K_max]
+    size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout)
+    size_t total;
+};
+
+// ---- launchers (return cudaError_t as int) --------------------------------
+int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const SlotMap& sm, float* qp, float* kp,
+                void* stream);
+int launch_score_select(const float* qp, const float* kp, const Geom& g, float* scores, int32_t* idx,
+                        void* stream);
+int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
+int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
+                const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,
+                uint32_t* status, uint64_t wait_limit_ns, void* stream);
+int launch_smma_prep(const float* S, const Geom& g, uint16_t* smma, void* stream);
+int launch_linear_read(const uint16_t* Q, const float* S, const float* z, const Geom& g, float* O, int accumulate,
+                       void* stream);
+int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int64_t head_stride, const Geom& g,
+                  float* S, float* z, uint32_t* status, uint64_t wait_limit_ns, void* stream);
+int launch_state_reset(float* S, float* z, const Geom& g, void* stream);
+int launch_selftest_wait(uint32_t* status, uint64_t limit_ns, void* stream);
+
+// Host helper: cuTensorMapEncodeTiled for a 3-D bf16 tensor with a
+// 128-byte swizzle.  dims/strides in elements/bytes (innermost first).
+int make_tmap_bf16_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                      uint64_t stride2_bytes, uint32_t box0, uint32_t box1);
+
+}  // namespace hf

@@ -1,0 +1,209 @@
+/*
+ * hf.h -- C ABI of the hybrid attention step of Hybrid Forcing
+ * ("Long-Horizon Streaming Video Generation via Hybrid Attention with
+ * Decoupled Distillation"), for NVIDIA B300 (sm_103a).
+ *
+ * The step has two paths whose outputs are summed (Spanish technical
+ * summary, section 2.A, "Atención Híbrida": the final output is the sum of
+ * the compressed linear history and the sparse local attention):
+ *   - block-sparse sliding-window softmax attention: query and key blocks
+ *     are mean-pooled and scored, and every query block attends only to its
+ *     top-K key blocks of the window (English technical summary, section
+ *     2.A.2 "Block-Sparse Sliding Window Attention");
+ *   - linear temporal attention: a read of a constant-size per-head state
+ *     S = sum phi(k) v^T, z = sum phi(k) that absorbs every frame evicted
+ *     from the window (English technical summary, section 2.A.1 "Linear
+ *     Temporal Attention"; arXiv abstract: "a compact key-value state to
+ *     incrementally absorb evicted tokens").  phi(x) = elu(x) + 1.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless marked (host).  The caller owns
+ *     every buffer, including the workspace; the library never allocates or
+ *     frees device memory.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All work is enqueued on it; nothing synchronises except
+ *     hf_get_device_status.
+ *   - Argument errors are returned synchronously before anything is
+ *     launched (HF_ERR_INVALID_ARG / HF_ERR_UNSUPPORTED).  A failed launch
+ *     returns HF_ERR_CUDA.  A kernel that gives up waiting (every wait in
+ *     every kernel is bounded) records HF_ERR_TIMEOUT in the workspace
+ *     status word, which hf_get_device_status reads.  hf_last_error() gives a
+ *     one-line description of the last error on the calling thread.
+ *   - All device pointers must be 16-byte aligned (TMA requirement).
+ *   - Results are deterministic: no floating-point atomics, fixed
+ *     reduction orders.
+ *
+ * Shapes (b = batch, H = heads, d = head_dim, N_f = tokens per latent
+ * frame, C = chunk frames, W = window frames INCLUDING the chunk,
+ * beta = block size, bpf = ceil(N_f / beta)):
+ *   Q      bf16 [b, H, C*N_f, d]         the chunk's queries (frames in order)
+ *   Kc, Vc bf16 [b, H, W, slot_stride, d] ring of W frame slots, slot_stride >= N_f
+ *   slot_map (host) int32 [n_win]        logical window frame w (0 = oldest,
+ *                                        the last C are the chunk) -> ring slot
+ *   S      fp32 [b, H, d, d]             row = feature of phi(k), column = value channel
+ *   z      fp32 [b, H, d]
+ *   nQB = C*bpf query blocks, nKB = n_win*bpf key blocks, K_eff = min(topk, nKB)
+ *   Blocks tile every frame separately from its first token; the last block
+ *   of a frame holds N_f - (bpf-1)*beta tokens.  Key block kb = w*bpf + j.
+ */
+#ifndef HF_H
+#define HF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HF_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define HF_API __attribute__((visibility("default")))
+#else
+#define HF_API
+#endif
+
+/* Limits checked on entry (HF_ERR_UNSUPPORTED beyond them). */
+#define HF_MAX_WINDOW_FRAMES 64
+#define HF_MAX_KEY_BLOCKS 1024
+
+typedef enum {
+    HF_OK = 0,
+    HF_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent sizes */
+    HF_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shapes */
+    HF_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    HF_ERR_TIMEOUT = 4,       /* a kernel's bounded wait ran out (device status) */
+    HF_ERR_DEVICE_CHECK = 5   /* a kernel found an inconsistent input (device status) */
+} hf_status;
+
+typedef struct {
+    int32_t batch;            /* >= 1 */
+    int32_t heads;            /* >= 1 */
+    int32_t head_dim;         /* 64 or 128 */
+    int32_t tokens_per_frame; /* N_f >= 1 */
+    int32_t window_frames;    /* W, includes the current chunk; 1..HF_MAX_WINDOW_FRAMES */
+    int32_t chunk_frames;     /* C, 1..W */
+    int32_t block_size;       /* beta: 32, 64 or 128 */
+    int32_t topk;             /* K >= 1; clamped to nKB */
+    float softmax_scale;      /* 0 -> 1/sqrt(head_dim) */
+    float lin_eps;            /* added to the linear-read denominator; e.g. 1e-6 */
+} hf_config;
+
+/* Version of this ABI (HF_ABI_VERSION). */
+HF_API int32_t hf_abi_version(void);
+
+/* Text for a status code (static storage). */
+HF_API const char *hf_status_string(hf_status s);
+
+/* One-line description of the last error returned on this thread. */
+HF_API const char *hf_last_error(void);
+
+/* Workspace bytes the forward/scoring/attention/absorb calls need for
+ * `cfg` (sized for a full window of cfg->window_frames frames).  The same
+ * workspace may be reused by every call on one stream; calls that run
+ * concurrently need separate workspaces.  It must be zeroed once before
+ * first use (its first 256 bytes are the device status word). */
+HF_API hf_status hf_workspace_size(const hf_config *cfg, size_t *bytes /* host */);
+
+/* S = 0, z = 0 (the empty state). */
+HF_API hf_status hf_state_reset(const hf_config *cfg, float *S, float *z, void *stream);
+
+/* Absorb evicted frames into the state (English technical summary, section
+ * 2.A.1: the state incrementally aggregates evicted frames):
+ *   S += sum_t phi(K_ev[t]) V_ev[t]^T,  z += sum_t phi(K_ev[t])
+ * for every (batch, head).  K_ev, V_ev: bf16 [b, H, n_ev_tokens, d].
+ * n_ev_tokens = 0 is a no-op.  tcgen05 GEMM with fp32 accumulation; phi(k)
+ * enters the MMA as a bf16 hi + lo pair, so S carries ~fp32 accuracy. */
+HF_API hf_status hf_absorb_evicted(const hf_config *cfg, float *S, float *z,
+                            const uint16_t *K_ev, const uint16_t *V_ev,
+                            int32_t n_ev_tokens, void *ws, void *stream);
+
+/* The same as hf_absorb_evicted, for evicted tokens that are not packed per
+ * head: token t of head h is the row at K_ev + (h * head_stride_tokens + t) * d
+ * (and likewise for V_ev), with head_stride_tokens >= n_ev_tokens.  This
+ * absorbs frames straight out of the key/value ring (frames contiguous in
+ * their slots, slot_stride = N_f) without a copy. */
+HF_API hf_status hf_absorb_evicted_strided(const hf_config *cfg, float *S, float *z,
+                                           const uint16_t *K_ev, const uint16_t *V_ev,
+                                           int32_t n_ev_tokens, int64_t head_stride_tokens,
+                                           void *ws, void *stream);
+
+/* Block importance scores (English technical summary, section 2.A.2):
+ *   scores[b,h,qb,kb] = <mean(Q block qb), mean(K block kb)>  (float32)
+ * Means are sequential float32 sums in token order divided by the token
+ * count; the dot is a sequential fused multiply-add chain over channels in
+ * ascending order; -0 becomes +0.  This fixed arithmetic makes the scores,
+ * and so the selected indices, bit-reproducible.
+ * scores: fp32 [b, H, nQB, nKB].  C <= n_win <= W. */
+HF_API hf_status hf_block_scores(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                          int32_t slot_stride, const int32_t *slot_map /* host */,
+                          int32_t n_win, float *scores, void *ws, void *stream);
+
+/* Top-K key blocks per query block (English technical summary, section
+ * 2.A.2: only the top-K most informative blocks are kept).  Order: score
+ * descending, then block index ascending (ties go to the lower index);
+ * the K_eff = min(topk, nKB) winners are written in ascending index order.
+ * scores: fp32 [b, H, nQB, nKB] (finite); idx: int32 [b, H, nQB, K_eff]. */
+HF_API hf_status hf_topk_blocks(const hf_config *cfg, const float *scores, int32_t nQB, int32_t nKB,
+                         int32_t *idx, void *stream);
+
+/* Block-sparse softmax attention (English technical summary, section
+ * 2.A.2): for every query token, softmax(scale * q.k) over the tokens of
+ * the key blocks selected for its query block, times V.  No other mask.
+ * idx: int32 [b, H, nQB, K_eff] ascending (as written by hf_topk_blocks).
+ * O_swa: fp32 [b, H, C*N_f, d].  tcgen05 MMAs, bf16 operands, fp32
+ * accumulation and softmax. */
+HF_API hf_status hf_sparse_swa_attn(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                             const uint16_t *Vc, int32_t slot_stride,
+                             const int32_t *slot_map /* host */, int32_t n_win,
+                             const int32_t *idx, float *O_swa, void *ws, void *stream);
+
+/* Linear read (English technical summary, section 2.A.1):
+ *   o_lin = phi(q)^T S / (phi(q)^T z + lin_eps)   (float32)
+ * O: fp32 [b, H, C*N_f, d]; accumulate != 0 adds o_lin to O, else stores. */
+HF_API hf_status hf_linear_read(const hf_config *cfg, const uint16_t *Q, const float *S,
+                         const float *z, float *O, int32_t accumulate, void *stream);
+
+/* The whole hybrid attention step for one chunk (both paths, summed; Spanish
+ * technical summary, section 2.A): pooling, scores, top-K, block-sparse
+ * attention and, fused into its epilogue, the linear read and the sum.
+ *   O = bf16( o_swa + o_lin )   bf16 [b, H, C*N_f, d], round to nearest even
+ * idx_out (optional, may be NULL): int32 [b, H, nQB, K_eff].
+ * S, z: the state AFTER absorbing the frames this chunk evicted. */
+HF_API hf_status hf_hybrid_forward(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                            const uint16_t *Vc, int32_t slot_stride,
+                            const int32_t *slot_map /* host */, int32_t n_win,
+                            const float *S, const float *z, uint16_t *O, int32_t *idx_out,
+                            void *ws, void *stream);
+
+/* hf_hybrid_forward with per-kernel timing: events[0..4] (cudaEvent_t
+ * handles created by the caller, or NULL for none) are recorded on `stream`
+ * before the pooling kernel, before the score/select kernel, before the state
+ * preparation kernel, before the attention kernel and after it.  The results
+ * are identical to hf_hybrid_forward. */
+HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                                            const uint16_t *Vc, int32_t slot_stride,
+                                            const int32_t *slot_map /* host */, int32_t n_win,
+                                            const float *S, const float *z, uint16_t *O,
+                                            int32_t *idx_out, void *ws, void *stream,
+                                            void *const *events /* host, 5 entries */);
+
+/* Synchronises `stream`, reads and clears the workspace status word.
+ * Returns HF_OK, HF_ERR_TIMEOUT or HF_ERR_DEVICE_CHECK (the first device-
+ * side error since the last call), or HF_ERR_CUDA.  *site (host, may be
+ * NULL) receives the code of the wait or check that failed. */
+HF_API hf_status hf_get_device_status(void *ws, void *stream, int32_t *site);
+
+/* Diagnostic: launches one tiny kernel that waits on a barrier nothing
+ * will ever release, with a limit of `limit_us` microseconds (1..100000),
+ * so that the bounded-wait path can be exercised without hanging anything;
+ * afterwards hf_get_device_status reports HF_ERR_TIMEOUT. */
+HF_API hf_status hf_selftest_wait_timeout(void *ws, int32_t limit_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HF_H */
