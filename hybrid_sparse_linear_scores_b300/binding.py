@@ -167,12 +167,21 @@ def hf_hybrid_forward(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx
 
 def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, events,
                                stream=None):
-    """events: 5 torch.cuda.Event objects (recorded between the kernels)."""
+    """events: 5 torch.cuda.Event objects (recorded between the kernels).
+    torch creates an event's CUDA handle on its first record and only
+    reports times for events it has recorded, so each event is recorded by
+    torch first; the library then records it again at its own point."""
+    st = _stream(stream)
+    import torch
+    ts = torch.cuda.ExternalStream(st.value) if st.value else torch.cuda.current_stream()
+    for e in events:
+        if e is not None:
+            e.record(ts)
     sm = _slots(slot_map)
     ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
     _check(lib().hf_hybrid_forward_profiled(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
                                             sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
-                                            _ptr(ws), _stream(stream), ev), "hf_hybrid_forward_profiled")
+                                            _ptr(ws), st, ev), "hf_hybrid_forward_profiled")
 
 
 def hf_get_device_status(ws, stream=None) -> tuple[int, int]:

@@ -10,6 +10,11 @@
 // phi(k) enters the MMA as a bf16 pair hi + lo (hi = rn(phi), lo =
 // rn(phi - hi)), two MMAs into one fp32 accumulator, so S keeps ~16 bits
 // more than a bf16 operand would give; z is summed in fp32 on CUDA cores.
+// The tensor-core accumulator only ever holds one 128-token tile: two TMEM
+// accumulators alternate, and the epilogue warps fold each finished tile
+// into fp32 registers with round-to-nearest adds while the next tile is
+// multiplied, so long absorbs do not accumulate the tensor core's internal
+// rounding over thousands of steps.
 //
 // One thread-block cluster (CL <= 8 CTAs) per head splits the tokens; the
 // CL partial states are summed through distributed shared memory in rank
@@ -42,8 +47,9 @@ struct AbsCfg {
     static constexpr int OFF_V = 4 * CHUNK;          // D/64 chunks
     static constexpr int STAGE = OFF_V + (D / 64) * CHUNK;
     static constexpr int OFF_MISC = NS * STAGE;
-    static constexpr int NBAR = 8;
+    static constexpr int NBAR = 12;
     static constexpr int OFF_ZP = OFF_MISC + 64 + 8 * NBAR;   // fp32 [8][D] z partials
+    static constexpr uint32_t TMEM_COLS = 256;                 // two accumulators of 128 columns
     static constexpr int SMEM = OFF_ZP + 8 * D * 4;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
     static constexpr int PITCH = D + 1;              // partial-state row pitch (floats)
@@ -52,7 +58,7 @@ struct AbsCfg {
     static constexpr int NTHR = 320;
 };
 
-enum { A_FULL = 0, A_PHI = 2, A_EMPTY = 4, A_ACC = 6, A_DRAIN = 7 };
+enum { A_FULL = 0, A_PHI = 2, A_EMPTY = 4, A_ACC_FULL = 6, A_ACC_FREE = 8, A_DRAIN = 10 };
 
 struct AbsParams {
     int BH, n, CL;
@@ -90,7 +96,10 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(&bar[A_PHI + s], 256);
             mbar_init(&bar[A_EMPTY + s], 1);
         }
-        mbar_init(&bar[A_ACC], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bar[A_ACC_FULL + b], 1);
+            mbar_init(&bar[A_ACC_FREE + b], 256);
+        }
         mbar_init(&bar[A_DRAIN], 1);
         misc[1] = 0;
         fence_mbar_init();
@@ -104,7 +113,7 @@ __global__ void __launch_bounds__(320, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) {
-        tmem_alloc(misc, 128);
+        tmem_alloc(misc, Cfg::TMEM_COLS);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -144,7 +153,9 @@ __global__ void __launch_bounds__(320, 1)
             bool ok = true;
             for (int i = 0; i < my_tiles && ok; ++i) {
                 const int s = i % Cfg::NS;
+                const int a = i & 1;
                 ok = mbar_wait(&bar[A_PHI + s], (i / Cfg::NS) & 1, wc, SITE_ABSORB_PHI);
+                if (ok && i >= 2) ok = mbar_wait(&bar[A_ACC_FREE + a], ((i >> 1) & 1) ^ 1, wc, SITE_ABSORB_ACC);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t st = smem_u32(smem + s * Cfg::STAGE);
@@ -153,14 +164,14 @@ __global__ void __launch_bounds__(320, 1)
                     const uint32_t a0 = st + (hl ? Cfg::OFF_LO : Cfg::OFF_K);
 #pragma unroll
                     for (int kk = 0; kk < Cfg::TT / 16; ++kk) {
-                        mma_ss(tmem, smem_desc(a0 + kk * 2048, Cfg::CHUNK, 1024),
+                        mma_ss(tmem + a * 128, smem_desc(a0 + kk * 2048, Cfg::CHUNK, 1024),
                                smem_desc(st + Cfg::OFF_V + kk * 2048, Cfg::CHUNK, 1024), Cfg::IDESC,
-                               (i > 0 || hl > 0 || kk > 0) ? 1u : 0u);
+                               (hl > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
                 mma_commit(&bar[A_EMPTY + s]);
+                mma_commit(&bar[A_ACC_FULL + a]);
             }
-            mma_commit(&bar[A_ACC]);
             mma_commit(&bar[A_DRAIN]);
             const uint32_t a = smem_u32(&bar[A_DRAIN]);
             const uint64_t t0 = globaltimer_ns();
@@ -180,11 +191,35 @@ __global__ void __launch_bounds__(320, 1)
         const int cp = t % NCP, rg = t / NCP;
         const int col = 2 * cp;
         const uint32_t coff = (uint32_t)(col / 64) * Cfg::CHUNK;
+        // accumulator drain: warp -> TMEM lane quarter, column half
+        constexpr int DC = D / 2;               // columns per draining thread
+        const int quarter = warp & 3;
+        const int chalf = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;
+        float racc[DC];
+#pragma unroll
+        for (int k = 0; k < DC; ++k) racc[k] = 0.0f;
         float z0 = 0.0f, z1 = 0.0f;
         bool ok = true;
+        auto drain = [&](int j) -> bool {
+            const int a = j & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[A_ACC_FULL + a], (j >> 1) & 1, wc, SITE_ABSORB_ACC)))
+                return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < DC; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + a * 128 + chalf * DC + c0, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) racc[c0 + k] = __fadd_rn(racc[c0 + k], __uint_as_float(v[k]));
+            }
+            tc_fence_before();
+            mbar_arrive(&bar[A_ACC_FREE + a]);
+            return true;
+        };
         for (int i = 0; i < my_tiles && ok; ++i) {
             const int s = i % Cfg::NS;
-            ok = mbar_wait(&bar[A_FULL + s], (i / Cfg::NS) & 1, wc, SITE_ABSORB_FULL);
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[A_FULL + s], (i / Cfg::NS) & 1, wc, SITE_ABSORB_FULL));
             if (!ok) break;
             uint8_t* st = smem + s * Cfg::STAGE;
             const int tok0 = (t_begin + i) * Cfg::TT;
@@ -209,29 +244,21 @@ __global__ void __launch_bounds__(320, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&bar[A_PHI + s]);
+            if (i >= 1) ok = drain(i - 1);
         }
+        if (ok && my_tiles > 0) ok = drain(my_tiles - 1);
         zp[rg * D + col] = z0;
         zp[rg * D + col + 1] = z1;
-        // ---- epilogue: accumulator -> partial state in shared memory ------
-        if (ok) ok = mbar_wait(&bar[A_ACC], 0, wc, SITE_ABSORB_ACC);
-        ok = __all_sync(0xFFFFFFFFu, ok);   // the TMEM loads below are warp-collective
-        float* part = reinterpret_cast<float*>(smem);   // [128][PITCH], over stage 0
+        // ---- partial state -> shared memory (over stage 0) ----------------
+        __syncwarp();
+        float* part = reinterpret_cast<float*>(smem);   // [128][PITCH]
+        // stage 0 may still be read by the producer's last TMA only if this
+        // CTA had a single tile in flight; every load was consumed above.
         if (ok) {
-            tc_fence_after();
-            const int quarter = warp & 3;
-            const int half = (warp - 2) >> 2;
-            const int row = quarter * 32 + lane;
-            for (int c0 = half * (D / 2); c0 < (half + 1) * (D / 2); c0 += 32) {
-                uint32_t v[32];
-                if (my_tiles > 0) {
-                    tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + c0, v);
-                } else {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = 0u;
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k) part[row * Cfg::PITCH + c0 + k] = __uint_as_float(v[k]);
-            }
+            for (int k = 0; k < DC; ++k) part[row * Cfg::PITCH + chalf * DC + k] = racc[k];
+        } else {
+            *wc.abort_flag = 1;
         }
     }
     tc_fence_before();
@@ -267,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
     cluster.sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 128);
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
 }
 

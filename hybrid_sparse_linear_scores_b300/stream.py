@@ -47,9 +47,9 @@ class HybridAttentionLayer:
 
     def frames_to_evict(self) -> list[int]:
         """Frames the next chunk pushes out of the window (oldest first)."""
-        n = max(0, self.frames + self.C - self.W)
-        first = self.frames - self.n_win()
-        return list(range(first, first + n))
+        first = self.frames - self.n_win()               # oldest frame in the window now
+        keep_from = max(0, self.frames + self.C - self.W)  # oldest frame after the chunk arrives
+        return list(range(first, max(first, keep_from)))
 
     # ---- the three phases of a step ----
     def absorb_evicted(self, stream=None) -> int:
@@ -68,7 +68,7 @@ class HybridAttentionLayer:
 
     def absorb_slots(self, first_slot: int, n_slots: int, stream=None):
         hb.hf_absorb_evicted_strided(self.cfg, self.S, self.z, self.Kc[:, first_slot], self.Vc[:, first_slot],
-                                     n_slots * self.nf if n_slots > 1 else self.nf, self.W * self.ss, self.ws,
+                                     n_slots * self.nf, self.W * self.ss, self.ws,
                                      stream)
 
     def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor):

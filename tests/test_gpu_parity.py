@@ -12,7 +12,7 @@ from hybrid_sparse_linear_scores_b300 import synth
 from hybrid_sparse_linear_scores_b300.stream import HybridAttentionLayer
 from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, SWEEP, Workload, frames_tensor, scaled
 
-from gpu_harness import Step, compare, config_of, flat, sample_rows
+from gpu_harness import STATE_REL_L2, Step, compare, compare_state, config_of, flat, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -131,8 +131,7 @@ def test_standalone_entry_points(cuda_device):
     compare(O_swa, ref["O"], max_abs=1e-2, rel_l2=3e-3, what="O_swa + O_lin")
     # the state itself
     S_ref, z_ref = st.oracle_state()
-    compare(L.S, S_ref, max_abs=1e-2, rel_l2=1e-5, what="S")
-    compare(L.z, z_ref, max_abs=1e-2, rel_l2=1e-6, what="z")
+    compare_state(L.S, L.z, S_ref, z_ref)
 
 
 @pytest.mark.parametrize("name", ["realistic", "wide"])
@@ -143,8 +142,7 @@ def test_absorb_full_config(name, cuda_device):
     st.layer.check_device_status()
     heads = [0, w.heads_total - 1]
     S_ref, z_ref = oracle.state_from_frames(flat(st.Kev[heads]).cpu(), flat(st.Vev[heads]).cpu())
-    compare(st.layer.S[heads], S_ref, max_abs=5e-2, rel_l2=1e-5, what="S")
-    compare(st.layer.z[heads], z_ref, max_abs=5e-2, rel_l2=1e-6, what="z")
+    compare_state(st.layer.S[heads], st.layer.z[heads], S_ref, z_ref)
 
 
 def test_incremental_absorb_matches_one_shot(cuda_device):
@@ -162,7 +160,7 @@ def test_incremental_absorb_matches_one_shot(cuda_device):
                              w.tokens_per_frame, L2.ws)
     torch.cuda.synchronize()
     d = (L1.S - L2.S).norm() / L1.S.norm()
-    assert float(d) < 1e-6
+    assert float(d) < STATE_REL_L2
 
 
 def test_deterministic_repeat(cuda_device):
