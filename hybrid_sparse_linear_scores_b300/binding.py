@@ -62,6 +62,8 @@ def lib():
             "hf_hybrid_forward": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P], _I),
             "hf_hybrid_forward_profiled": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P,
                                             ctypes.POINTER(ctypes.c_void_p)], _I),
+            "hf_hybrid_forward_noalloc": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P,
+                                           ctypes.POINTER(ctypes.c_void_p), _P], _I),
             "hf_get_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
             "hf_selftest_wait_timeout": ([_P, _I, _P], _I),
         }
@@ -182,6 +184,19 @@ def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, 
     _check(lib().hf_hybrid_forward_profiled(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
                                             sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
                                             _ptr(ws), st, ev), "hf_hybrid_forward_profiled")
+
+
+def hf_hybrid_forward_noalloc(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, stream=None):
+    """hf_hybrid_forward without a workspace argument (the library's static
+    device scratch stands in for it).  Returns the device address of the
+    scratch's status word, to pass as ``ws`` to :func:`hf_get_device_status`."""
+    sm = _slots(slot_map)
+    status_word = ctypes.c_void_p(0)
+    _check(lib().hf_hybrid_forward_noalloc(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
+                                           sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
+                                           ctypes.byref(status_word), _stream(stream)),
+           "hf_hybrid_forward_noalloc")
+    return status_word.value
 
 
 def hf_get_device_status(ws, stream=None) -> tuple[int, int]:

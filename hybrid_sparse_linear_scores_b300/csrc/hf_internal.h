@@ -85,6 +85,10 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
 int launch_state_reset(float* S, float* z, const Geom& g, void* stream);
 int launch_selftest_wait(uint32_t* status, uint64_t limit_ns, void* stream);
 
+// Records a printf-style message as the calling thread's hf_last_error()
+// text and returns `code`.
+hf_status set_last_error(hf_status code, const char* fmt, ...);
+
 // Host helper: cuTensorMapEncodeTiled for a 3-D bf16 tensor with a
 // 128-byte swizzle.  dims/strides in elements/bytes (innermost first).
 int make_tmap_bf16_3d(void* tmap_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,

@@ -190,6 +190,51 @@ HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t
                                             int32_t *idx_out, void *ws, void *stream,
                                             void *const *events /* host, 5 entries */);
 
+/* Size of the static device scratch that hf_hybrid_forward_noalloc uses in
+ * place of a workspace: 16 MiB, enough for hf_workspace_size() of a 40-head,
+ * d = 128 layer with 1560-token frames, a 9-frame window, 3-frame chunks and
+ * block 64 (about 9.5 MB). */
+#define HF_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* hf_hybrid_forward for callers that cannot allocate device memory.  The
+ * paper has no counterpart: this is a deployment convenience.
+ *
+ * Some callers have no way to hand over a workspace: a custom-operator
+ * interface that passes only inputs, outputs and a stream; code that runs
+ * while a stream is being captured into a CUDA graph, where cudaMalloc is
+ * not allowed; an engine that keeps every byte of the device in its own
+ * pool.  This entry point takes the same arguments as hf_hybrid_forward
+ * except `ws`, and runs the same kernels with the workspace placed in a
+ * static device array of HF_NOALLOC_SCRATCH_BYTES that the library defines.
+ * The caller still passes (and owns) every input and output.  Nothing is
+ * allocated or freed: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ *   - Memory: every device that loads the library holds one copy of the
+ *     array until the process exits.
+ *   - Limit: a configuration whose hf_workspace_size() exceeds
+ *     HF_NOALLOC_SCRATCH_BYTES is rejected with HF_ERR_UNSUPPORTED before
+ *     anything is launched; use hf_hybrid_forward for it.
+ *   - Set-up: the first call on a device (the calling thread's current
+ *     device, which must be the device of `stream` and of the buffers) looks
+ *     up the array's device address with cudaGetSymbolAddress, which may load
+ *     the library's module on that device.  Make that first call before any
+ *     stream capture.  Later calls on the device reuse the address.
+ *   - Sharing: every call on a device uses the same array, and the array
+ *     keeps whatever the last call left in it.  All of it is rewritten before
+ *     it is read except the status word, which starts at zero when the
+ *     library loads and is cleared by hf_get_device_status.  Two calls whose
+ *     kernels may overlap on the GPU (different streams with no ordering
+ *     between them) race on the array and give wrong results: order them.
+ *   - Device-side errors (a bounded wait that ran out, a bad index) go to
+ *     the array's status word.  *status_word (host, may be NULL) receives its
+ *     device address; pass that address as `ws` to hf_get_device_status.
+ */
+HF_API hf_status hf_hybrid_forward_noalloc(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                                           const uint16_t *Vc, int32_t slot_stride,
+                                           const int32_t *slot_map /* host */, int32_t n_win,
+                                           const float *S, const float *z, uint16_t *O, int32_t *idx_out,
+                                           void **status_word /* host, may be NULL */, void *stream);
+
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns HF_OK, HF_ERR_TIMEOUT or HF_ERR_DEVICE_CHECK (the first device-
  * side error since the last call), or HF_ERR_CUDA.  *site (host, may be
