@@ -1,7 +1,8 @@
 """Device state of one streaming hybrid attention layer, driven through the C ABI.
 
 The layer owns (in device memory, allocated by torch):
-  - the key/value ring of W frame slots, [BH, W, slot_stride, d] bf16,
+  - the key/value ring of frame slots, [BH, R, slot_stride, d] bf16, with
+    R = W + spare_slots (W = window frames, the chunk included),
   - the linear state S [BH, d, d] and z [BH, d] (fp32),
   - the library workspace.
 A chunk of C frames is processed as in Hybrid Forcing's streaming loop
@@ -10,10 +11,16 @@ window are absorbed into the compact state): first the frames this chunk
 evicts are absorbed into (S, z) straight from their ring slots, then the
 chunk's keys/values take those slots, then the hybrid forward runs over the
 window.  Logical window order (oldest first) is passed as the slot map, so
-no frame is ever moved.
+no frame is ever moved.  Frame f lives in slot f mod R.
+
+With spare_slots = C the next chunk's keys/values can be copied in while the
+current chunk's forward still reads the window (HostStreamer below).  The C
+ABI sees a ring of R slots (its config's window_frames = R) and a window of
+n_win <= W frames; the top-K count is the config's fixed topk.
 """
 
 from __future__ import annotations
+
 
 import torch
 
@@ -21,60 +28,69 @@ from . import binding as hb
 
 
 class HybridAttentionLayer:
-    def __init__(self, cfg: hb.HFConfig, device="cuda", slot_stride: int | None = None):
-        self.cfg = cfg
+    def __init__(self, cfg: hb.HFConfig, device="cuda", slot_stride: int | None = None, spare_slots: int = 0):
+        self.window = cfg.window_frames                  # W: frames attended (chunk included)
+        self.R = cfg.window_frames + spare_slots         # ring slots
+        self.cfg = hb.HFConfig.from_buffer_copy(cfg)     # the ABI's view: window_frames = ring slots
+        self.cfg.window_frames = self.R
         self.device = torch.device(device)
         self.BH = cfg.batch * cfg.heads
-        self.W = cfg.window_frames
+        self.W = self.R
         self.C = cfg.chunk_frames
         self.nf = cfg.tokens_per_frame
         self.d = cfg.head_dim
         self.ss = slot_stride or self.nf
-        self.Kc = torch.zeros((self.BH, self.W, self.ss, self.d), dtype=torch.bfloat16, device=self.device)
+        self.Kc = torch.zeros((self.BH, self.R, self.ss, self.d), dtype=torch.bfloat16, device=self.device)
         self.Vc = torch.zeros_like(self.Kc)
         self.S = torch.zeros((self.BH, self.d, self.d), dtype=torch.float32, device=self.device)
         self.z = torch.zeros((self.BH, self.d), dtype=torch.float32, device=self.device)
-        self.ws = torch.zeros(hb.hf_workspace_size(cfg), dtype=torch.uint8, device=self.device)
+        self.ws = torch.zeros(hb.hf_workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
         self.frames = 0
 
     # ---- window bookkeeping (host) ----
     def n_win(self) -> int:
-        return min(self.W, self.frames)
+        return min(self.window, self.frames)
 
     def slot_map(self) -> list[int]:
         first = self.frames - self.n_win()
-        return [(first + w) % self.W for w in range(self.n_win())]
+        return [(first + w) % self.R for w in range(self.n_win())]
 
     def frames_to_evict(self) -> list[int]:
         """Frames the next chunk pushes out of the window (oldest first)."""
-        first = self.frames - self.n_win()               # oldest frame in the window now
-        keep_from = max(0, self.frames + self.C - self.W)  # oldest frame after the chunk arrives
+        first = self.frames - self.n_win()                      # oldest frame in the window now
+        keep_from = max(0, self.frames + self.C - self.window)  # oldest frame after the chunk arrives
         return list(range(first, max(first, keep_from)))
+
+    def _slot_runs(self, frames) -> list[list[int]]:
+        """Frames grouped into runs of consecutive ring slots."""
+        runs: list[list[int]] = []
+        for f in frames:
+            s = f % self.R
+            if runs and self.ss == self.nf and runs[-1][-1] + 1 == s:
+                runs[-1].append(s)
+            else:
+                runs.append([s])
+        return runs
 
     # ---- the three phases of a step ----
     def absorb_evicted(self, stream=None) -> int:
         """Absorb the frames the next chunk evicts, from their ring slots."""
         frames = self.frames_to_evict()
-        runs: list[list[int]] = []
-        for f in frames:   # group into runs of consecutive slots (one call each)
-            s = f % self.W
-            if runs and self.ss == self.nf and runs[-1][-1] + 1 == s:
-                runs[-1].append(s)
-            else:
-                runs.append([s])
-        for run in runs:
+        for run in self._slot_runs(frames):
             self.absorb_slots(run[0], len(run), stream)
         return len(frames)
 
     def absorb_slots(self, first_slot: int, n_slots: int, stream=None):
         hb.hf_absorb_evicted_strided(self.cfg, self.S, self.z, self.Kc[:, first_slot], self.Vc[:, first_slot],
-                                     n_slots * self.nf, self.W * self.ss, self.ws,
-                                     stream)
+                                     n_slots * self.nf, self.R * self.ss, self.ws, stream)
+
+    def chunk_slots(self) -> list[int]:
+        """Ring slots of the next chunk's frames."""
+        return [(self.frames + c) % self.R for c in range(self.C)]
 
     def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor):
         """K_new, V_new: [BH, C, N_f, d] bf16 for the next C frames."""
-        for c in range(self.C):
-            slot = (self.frames + c) % self.W
+        for c, slot in enumerate(self.chunk_slots()):
             self.Kc[:, slot, :self.nf].copy_(K_new[:, c])
             self.Vc[:, slot, :self.nf].copy_(V_new[:, c])
         self.frames += self.C
@@ -89,7 +105,95 @@ class HybridAttentionLayer:
         self.write_chunk(K_new, V_new)
         self.forward(Q, O, idx_out, stream)
 
+    # ---- checkpoint / resume ----
+    def state_dict(self) -> dict:
+        """Everything the stream needs to continue: ring, state, frame count."""
+        return {"Kc": self.Kc.clone(), "Vc": self.Vc.clone(), "S": self.S.clone(), "z": self.z.clone(),
+                "frames": self.frames}
+
+    def load_state_dict(self, sd: dict):
+        self.Kc.copy_(sd["Kc"])
+        self.Vc.copy_(sd["Vc"])
+        self.S.copy_(sd["S"])
+        self.z.copy_(sd["z"])
+        self.frames = int(sd["frames"])
+
     def check_device_status(self, stream=None):
         rc, site = hb.hf_get_device_status(self.ws, stream)
         if rc != hb.HF_OK:
             raise hb.HFError(rc, "device status", f"site {site}: {hb.lib().hf_last_error().decode()}")
+
+
+class HostStreamer:
+    """Streams chunks from pinned host memory through a layer, overlapping the
+    host<->device copies with compute.
+
+    The layer needs spare_slots >= chunk_frames.  Frame f lives in slot
+    f mod R (R = W + spare), so the slots the next chunk takes held frames
+    that the current step absorbs; once that absorb is done, the next chunk's
+    copy-in runs while the current forward still reads the window.  Q and O
+    are double-buffered on the device.  Three streams (compute,
+    host->device, device->host) ordered by events.
+
+    push(Qh, Kh, Vh, Oh): Qh, Oh [BH, C*N_f, d] and Kh, Vh [BH, C, N_f, d],
+    bf16 pinned host tensors.  Per chunk, on the compute stream: absorb the
+    frames the chunk's arrival evicted (still in their slots), then, once the
+    chunk's copies have landed, the hybrid forward; then O is copied back.
+    Oh is valid after synchronize().
+    """
+
+    def __init__(self, layer: HybridAttentionLayer):
+        assert layer.R >= layer.window + layer.C, "HostStreamer needs spare_slots >= chunk_frames"
+        self.L = layer
+        dev = layer.device
+        shape = (layer.BH, layer.C * layer.nf, layer.d)
+        self.Qd = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.Od = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.cs = torch.cuda.Stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.n = 0
+        self.ev_h2d = [torch.cuda.Event() for _ in range(2)]
+        self.ev_fwd = [torch.cuda.Event() for _ in range(2)]
+        self.ev_d2h = [torch.cuda.Event() for _ in range(2)]
+        self.ev_absorb = torch.cuda.Event()
+        self.h2d_bytes = 0
+        self.d2h_bytes = 0
+
+    def push(self, Qh, Kh, Vh, Oh):
+        L, b = self.L, self.n % 2
+        # 1. copy-in: the chunk's slots were absorbed by the previous step;
+        #    Qd[b] was last read by the forward two chunks back.
+        slots = L.chunk_slots()
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.ev_absorb)
+            self.h2d.wait_event(self.ev_fwd[b])
+            self.Qd[b].copy_(Qh, non_blocking=True)
+            for c, slot in enumerate(slots):
+                L.Kc[:, slot, :L.nf].copy_(Kh[:, c], non_blocking=True)
+                L.Vc[:, slot, :L.nf].copy_(Vh[:, c], non_blocking=True)
+            self.ev_h2d[b].record(self.h2d)
+        self.h2d_bytes += (Qh.numel() + Kh.numel() + Vh.numel()) * 2
+        # 2. compute: absorb the frames this chunk's arrival evicts (they are
+        #    still in their slots), then the forward once the copies landed.
+        evicted = L.frames_to_evict()
+        L.frames += L.C
+        for run in L._slot_runs(evicted):
+            L.absorb_slots(run[0], len(run), self.cs)
+        self.ev_absorb.record(self.cs)
+        self.cs.wait_event(self.ev_h2d[b])
+        self.cs.wait_event(self.ev_d2h[b])            # Od[b] has been read back
+        L.forward(self.Qd[b], self.Od[b], None, self.cs)
+        self.ev_fwd[b].record(self.cs)
+        # 3. copy-out
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.ev_fwd[b])
+            Oh.copy_(self.Od[b], non_blocking=True)
+            self.ev_d2h[b].record(self.d2h)
+        self.d2h_bytes += Oh.numel() * 2
+        self.n += 1
+
+    def synchronize(self):
+        self.d2h.synchronize()
+        self.cs.synchronize()
+        self.h2d.synchronize()

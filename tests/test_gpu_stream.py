@@ -1,0 +1,131 @@
+"""Streaming on the GPU: the long-horizon stream (80 chunks of 3 frames, 240
+frames) against the oracle at sampled steps, checkpoint/resume, and the
+host streamer (copies overlapped with compute) against the plain layer.
+
+Hybrid Forcing, English technical summary, section 2.A.1: the state absorbs
+every frame evicted from the window, at constant size whatever the length
+of the video."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hybrid_sparse_linear_scores_b300 import synth
+from hybrid_sparse_linear_scores_b300.stream import HostStreamer, HybridAttentionLayer
+from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, Workload, frames_tensor
+
+from gpu_harness import compare, compare_state, config_of, flat, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def chunk_inputs(w: Workload, s: int, dev):
+    Kn = frames_tensor(w, synth.STREAM_K, w.chunk(s), dev)
+    Vn = frames_tensor(w, synth.STREAM_V, w.chunk(s), dev)
+    Q = flat(frames_tensor(w, synth.STREAM_Q, w.chunk(s), dev))
+    return Q, Kn, Vn
+
+
+def test_long_horizon_stream(cuda_device):
+    """240 frames through the layer's ring: at steps {0, 1, 2, 3, 40, 79} all
+    selected indices are exact and sampled rows of three heads match the
+    oracle, whose state is absorbed frame by frame in fp64 alongside; the
+    device state matches it at the end; the state never changes size."""
+    w = CONFIGS["stream"]
+    check = {0, 1, 2, 3, 40, 79}
+    heads = [0, 5, 11]
+    cfg = config_of(w, w.steps - 1)
+    L = HybridAttentionLayer(cfg, cuda_device)
+    state_bytes = L.S.numel() * 4 + L.z.numel() * 4
+    S_ref = np.zeros((len(heads), w.head_dim, w.head_dim))
+    z_ref = np.zeros((len(heads), w.head_dim))
+    for s in range(w.steps):
+        cfg.topk = w.k_for(s)
+        L.cfg.topk = w.k_for(s)
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        O = torch.empty_like(Q)
+        idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+        L.step(Q, Kn, Vn, O, idx)
+        new = w.newly_absorbed(s)
+        if new:
+            Ke = flat(frames_tensor(w, synth.STREAM_K, new, cuda_device)[heads]).cpu()
+            Ve = flat(frames_tensor(w, synth.STREAM_V, new, cuda_device)[heads]).cpu()
+            S_ref, z_ref = oracle.state_from_frames(Ke, Ve, S_ref, z_ref)
+        assert L.S.numel() * 4 + L.z.numel() * 4 == state_bytes
+        if s not in check:
+            continue
+        torch.cuda.synchronize()
+        L.check_device_status()
+        win = w.window(s)
+        Kw = flat(frames_tensor(w, synth.STREAM_K, win, cuda_device)).cpu()
+        Vw = flat(frames_tensor(w, synth.STREAM_V, win, cuda_device)).cpu()
+        geo = dict(C=w.chunk_frames, n_win=w.n_win(s), nf=w.tokens_per_frame, beta=w.block_size, k=w.k_for(s))
+        ref_idx = oracle.hybrid_forward(Q.cpu(), Kw, Vw, None, None, rows=np.array([0], np.int32), **geo)["idx"]
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx, err_msg=f"step {s}")
+        rows = sample_rows(w, 48, seed=s)
+        have_state = w.absorbed_before(s) > 0
+        ref = oracle.hybrid_forward(Q[heads].cpu(), Kw[heads], Vw[heads], S_ref if have_state else None,
+                                    z_ref if have_state else None, rows=rows, **geo)
+        compare(O[heads][:, rows], ref["O"], what=f"stream step {s}")
+    compare_state(L.S[heads], L.z[heads], S_ref, z_ref)
+
+
+def test_checkpoint_resume_is_bit_identical(cuda_device):
+    """Save the streaming state after 3 chunks, restore it into a fresh layer
+    and continue: every later output and index is bit-identical to the
+    uninterrupted run (all kernels are deterministic)."""
+    w = Workload("ckpt", 1, 2, 128, 200, 2, 6, 64, seed=31, recipe="drift", topk_frac=0.3, steps=8)
+    cfg = config_of(w, w.steps - 1)
+    A = HybridAttentionLayer(cfg, cuda_device)
+    outs_a, saved = [], None
+    for s in range(w.steps):
+        A.cfg.topk = w.k_for(s)
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        O = torch.empty_like(Q)
+        idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+        A.step(Q, Kn, Vn, O, idx)
+        outs_a.append((O, idx))
+        if s == 2:
+            torch.cuda.synchronize()
+            saved = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in A.state_dict().items()}
+    B = HybridAttentionLayer(cfg, cuda_device)
+    B.load_state_dict(saved)
+    for s in range(3, w.steps):
+        B.cfg.topk = w.k_for(s)
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        O = torch.empty_like(Q)
+        idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+        B.step(Q, Kn, Vn, O, idx)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, outs_a[s][1]), f"step {s}"
+        assert torch.equal(O.view(torch.int16), outs_a[s][0].view(torch.int16)), f"step {s}"
+
+
+def test_host_streamer_matches_layer_steps(cuda_device):
+    """Chunks pushed from pinned host memory through HostStreamer (ring with
+    spare slots, copies on their own streams) give bit-identical outputs to
+    the plain layer stepping the same chunks."""
+    w = Workload("hs", 1, 3, 128, 300, 3, 9, 64, seed=41, recipe="drift", topk=20, steps=7)
+    cfg = config_of(w, w.steps - 1)
+    ref = HybridAttentionLayer(cfg, cuda_device)
+    L = HybridAttentionLayer(cfg, cuda_device, spare_slots=w.chunk_frames)
+    hs = HostStreamer(L)
+    outs_ref, outs_host, keep = [], [], []
+    for s in range(w.steps):
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        O = torch.empty_like(Q)
+        ref.step(Q, Kn, Vn, O)
+        outs_ref.append(O)
+        Oh = torch.empty(Q.shape, dtype=Q.dtype).pin_memory()
+        host = (Q.cpu().pin_memory(), Kn.cpu().pin_memory(), Vn.cpu().pin_memory())
+        keep.append(host)                   # host buffers live until the copies are done
+        hs.push(*host, Oh)
+        outs_host.append(Oh)
+    hs.synchronize()
+    torch.cuda.synchronize()
+    ref.check_device_status()
+    L.check_device_status()
+    for s in range(w.steps):
+        assert torch.equal(outs_host[s].view(torch.int16), outs_ref[s].cpu().view(torch.int16)), f"chunk {s}"
+    assert torch.equal(L.S, ref.S) and torch.equal(L.z, ref.z)
