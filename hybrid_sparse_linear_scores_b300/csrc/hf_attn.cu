@@ -273,9 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&bar[B_Q], 1);
                 for (int s = 0; s < Cfg::NR; ++s) {
                     mbar_init(&bar[B_K_FULL + s], 1);
-                    mbar_init(&bar[B_K_EMPTY + s], 2);   // both MMA threads release a stage
+                    mbar_init(&bar[B_K_EMPTY + s], 1);
                     mbar_init(&bar[B_V_FULL + s], 1);
-                    mbar_init(&bar[B_V_EMPTY + s], 2);
+                    mbar_init(&bar[B_V_EMPTY + s], 1);
                 }
                 for (int t = 0; t < 2; ++t) {
                     mbar_init(&bar[B_S_FULL + t], 1);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_init(&bar[B_LIN_DONE + t], 1);
                 }
                 mbar_init(&bar[B_LIN_FULL], 1);
-                mbar_init(&bar[B_DRAIN], 2);
+                mbar_init(&bar[B_DRAIN], 1);
                 misc[M_LAST] = 0;
                 misc[M_LAST + 1] = 0;
                 fence_mbar_init();
@@ -413,92 +413,114 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = max(0, issued - Cfg::NR); r < issued; ++r)
                     drain_wait(&bar[B_V_FULL + r % Cfg::NR], (r / Cfg::NR) & 1, p.wait_limit_ns);
                 if (!ok) *wc.abort_flag = 1;
-            } else if ((warp == 1 || warp == 3) && lane == 0) {
-                // ---------- MMA issuer of tile t (warp 1: A, warp 3: B) ----------
-                // Each tile has its own issuing thread, so one tile's MMAs are queued
-                // while the other thread waits for its softmax.  Both threads wait for
-                // every round's key and value stages and both release them (the empty
-                // barriers count two arrivals), so neither runs more than a ring ahead.
-                const int t = warp >> 1;
+            } else if (warp == 1 && lane == 0) {
+                // ---------- MMA issuer ----------
+                // Batches in the order A(-1) B(-1) A(0) B(0) A(1) ..., batch t(r) =
+                // P V_t(r) followed by Q K^T_t(r+1) (S_t is free again once P V_t(r) has
+                // been issued: the tensor core executes in issue order).  Each tile's
+                // softmax then runs while the tensor core works on the other tile's
+                // batch.  The MMA queue holds only a few MMAs, so the thread keeps the
+                // work between batches short: round codes are read ahead, and each
+                // round's key and value stages are waited for once.
                 bool ok = mbar_wait(&bar[B_Q], 0, wc, SITE_ATTN_Q);
                 tc_fence_after();
-                // base descriptors (start addresses advance in 16-byte units): the Q tile and
+                // base descriptors (start addresses advance in 16-byte units): Q tiles and
                 // the key ring K-major, the value ring MN-major (64-column chunks CHUNK apart)
-                const uint64_t q_desc = smem_desc(smem_u32(smem + Cfg::OFF_Q + t * Cfg::Q_BYTES), 16, 1024);
+                const uint64_t q_desc0 = smem_desc(smem_u32(smem + Cfg::OFF_Q), 16, 1024);
+                const uint64_t q_desc1 = smem_desc(smem_u32(smem + Cfg::OFF_Q + Cfg::Q_BYTES), 16, 1024);
                 const uint64_t k_desc = smem_desc(smem_u32(sK), 16, 1024);
                 const uint64_t v_desc = smem_desc(smem_u32(sV), Cfg::CHUNK, 1024);
-                const int last_round = ((int)misc[M_LAST + t] - 1) >> 1;
-                const uint32_t o_tm = tmem + 256 * t;
-                const uint32_t s_tm = o_tm + 128;
-                int cnt = 0;
-                bool first = true;
+                const int last_round0 = ((int)misc[M_LAST + 0] - 1) >> 1;
+                const int last_round1 = ((int)misc[M_LAST + 1] - 1) >> 1;
+                int cnt0 = 0, cnt1 = 0;
+                bool first0 = true, first1 = true;
+                int k_round = -1, v_round = -1;   // last round whose key / value stage was waited for
                 // m: the tile's slabs of round r (bit i = slab i), from the round code
-                auto issue_qk = [&](int r, uint32_t m) -> bool {
+                auto issue_qk = [&](int r, int t, uint32_t m) -> bool {
+                    if (m == 0) return true;
                     const int s = r % Cfg::NR;
-                    if (!mbar_wait(&bar[B_K_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
-                    if (m != 0) {
-                        tc_fence_after();
-                        // both slabs: one N = 128 operand; one slab: its 64 rows
-                        const uint64_t kd =
-                            k_desc + (uint64_t)((s * Cfg::RS_BYTES + (m == 2u ? Cfg::SLAB * 128 : 0)) >> 4);
-                        const uint32_t idesc = m == 3u ? Cfg::IDESC_QK128 : Cfg::IDESC_QK64;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(s_tm, q_desc + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
-                                   kd + (uint64_t)(((kk >> 2) * Cfg::CHUNK + (kk & 3) * 32) >> 4), idesc,
-                                   kk > 0 ? 1u : 0u);
-                        mma_commit(&bar[B_S_FULL + t]);
+                    if (r > k_round) {
+                        if (!mbar_wait(&bar[B_K_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        k_round = r;
                     }
-                    mma_commit(&bar[B_K_EMPTY + s]);
+                    tc_fence_after();
+                    const uint64_t qd = t ? q_desc1 : q_desc0;
+                    // both slabs: one N = 128 operand; one slab: its 64 rows
+                    const uint64_t kd =
+                        k_desc + (uint64_t)((s * Cfg::RS_BYTES + (m == 2u ? Cfg::SLAB * 128 : 0)) >> 4);
+                    const uint32_t idesc = m == 3u ? Cfg::IDESC_QK128 : Cfg::IDESC_QK64;
+                    const uint32_t dt = tmem + 256 * t + 128;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(dt, qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
+                               kd + (uint64_t)(((kk >> 2) * Cfg::CHUNK + (kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
+                    mma_commit(&bar[B_S_FULL + t]);
                     return true;
                 };
-                auto issue_pv = [&](int r, uint32_t m) -> bool {
+                auto issue_pv = [&](int r, int t, uint32_t m) -> bool {
+                    if (m == 0) return true;
+                    int& cnt = t ? cnt1 : cnt0;
+                    bool& first = t ? first1 : first0;
+                    if (!mbar_wait(&bar[B_P_FULL + t], cnt & 1, wc, SITE_ATTN_P_FULL)) return false;
+                    ++cnt;
                     const int s = r % Cfg::NR;
-                    if (m != 0) {
-                        if (!mbar_wait(&bar[B_P_FULL + t], cnt & 1, wc, SITE_ATTN_P_FULL)) return false;
-                        ++cnt;
+                    if (r > v_round) {
+                        if (!mbar_wait(&bar[B_V_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        v_round = r;
                     }
-                    if (!mbar_wait(&bar[B_V_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
-                    if (m != 0) {
-                        tc_fence_after();
-                        const int n = m == 3u ? 2 : 1;
+                    tc_fence_after();
+                    const int n = m == 3u ? 2 : 1;
+                    const uint32_t o_tm = tmem + 256 * t;
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            if (j >= n) break;
-                            const int i = (m == 2u) ? 1 : j;   // slab of the round; P columns [32j, 32j + 32)
-                            const uint64_t vd = v_desc + (uint64_t)((s * Cfg::RS_BYTES + i * Cfg::SLAB * 128) >> 4);
+                    for (int j = 0; j < 2; ++j) {
+                        if (j >= n) break;
+                        const int i = (m == 2u) ? 1 : j;   // slab of the round; P columns [32j, 32j + 32)
+                        const uint64_t vd = v_desc + (uint64_t)((s * Cfg::RS_BYTES + i * Cfg::SLAB * 128) >> 4);
+                        const uint32_t at = o_tm + 128 + 32 * j;
 #pragma unroll
-                            for (int kk = 0; kk < Cfg::SLAB / 16; ++kk)
-                                mma_ts(o_tm, s_tm + 32 * j + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), Cfg::IDESC_PV,
-                                       (first && j == 0 && kk == 0) ? 0u : 1u);
-                        }
-                        first = false;
-                        if (r == last_round) mma_commit(&bar[B_O_DONE + t]);
+                        for (int kk = 0; kk < Cfg::SLAB / 16; ++kk)
+                            mma_ts(o_tm, at + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), Cfg::IDESC_PV,
+                                   (first && j == 0 && kk == 0) ? 0u : 1u);
                     }
-                    mma_commit(&bar[B_V_EMPTY + s]);
+                    first = false;
+                    if (r == (t ? last_round1 : last_round0)) mma_commit(&bar[B_O_DONE + t]);
                     return true;
                 };
                 // round codes are read one round ahead of their use
                 uint32_t c_cur = sCode[0];
                 uint32_t c_nxt = n_rounds > 1 ? sCode[1] : 0u;
-                if (ok) ok = issue_qk(0, tile_bits(c_cur, t));
+                if (ok) ok = issue_qk(0, 0, tile_bits(c_cur, 0)) && issue_qk(0, 1, tile_bits(c_cur, 1));
+                if (ok) mma_commit(&bar[B_K_EMPTY + 0]);
                 for (int r = 0; ok && r < n_rounds; ++r) {
                     const uint32_t c_nn = r + 2 < n_rounds ? sCode[r + 2] : 0u;
-                    ok = issue_pv(r, tile_bits(c_cur, t));
-                    if (ok && r + 1 < n_rounds) ok = issue_qk(r + 1, tile_bits(c_nxt, t));
+                    const bool more = r + 1 < n_rounds;
+                    ok = issue_pv(r, 0, tile_bits(c_cur, 0));
+                    if (ok && more) ok = issue_qk(r + 1, 0, tile_bits(c_nxt, 0));
+                    if (ok) ok = issue_pv(r, 1, tile_bits(c_cur, 1));
+                    if (!ok) break;
+                    mma_commit(&bar[B_V_EMPTY + r % Cfg::NR]);
+                    if (more) {
+                        ok = issue_qk(r + 1, 1, tile_bits(c_nxt, 1));
+                        if (ok) mma_commit(&bar[B_K_EMPTY + (r + 1) % Cfg::NR]);
+                    }
                     c_cur = c_nxt;
                     c_nxt = c_nn;
                 }
-                if (FUSED && ok && nblk[t] > 0) {
-                    ok = mbar_wait(&bar[B_LIN_FULL], 0, wc, SITE_ATTN_LIN) && mbar_wait(&bar[B_PHIQ + t], 0, wc, SITE_ATTN_PHIQ);
-                    if (ok) {
+                if (FUSED && ok) {
+                    ok = mbar_wait(&bar[B_LIN_FULL], 0, wc, SITE_ATTN_LIN);
+                    const uint64_t l_desc = smem_desc(smem_u32(sK), D * 128, 1024);
+                    for (int t = 0; ok && t < 2; ++t) {
+                        if (nblk[t] == 0) continue;
+                        ok = mbar_wait(&bar[B_PHIQ + t], 0, wc, SITE_ATTN_PHIQ);
+                        if (!ok) break;
                         tc_fence_after();
-                        const uint64_t l_desc = smem_desc(smem_u32(sK), D * 128, 1024);
+                        const uint64_t qd = t ? q_desc1 : q_desc0;
 #pragma unroll
                         for (int hl = 0; hl < 2; ++hl) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(s_tm, q_desc + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
+                                mma_ss(tmem + 256 * t + 128,
+                                       qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
                                        l_desc + (uint64_t)((hl * (D * D * 2) + kk * 2048) >> 4), Cfg::IDESC_LIN,
                                        (hl > 0 || kk > 0) ? 1u : 0u);
                         }
