@@ -8,16 +8,19 @@ workload ("realistic": batch 1, 12 heads, head_dim 128, 1560 tokens per
 latent frame, 3-frame chunk, 9-frame window, block 64, top-K 25 % = 57 of
 225 key blocks, 30 frames already in the linear state):
   hf_absorb_evicted_strided  (the 3 frames the chunk evicts, from the ring)
-  hf_hybrid_forward          (pool -> score/top-K -> state prep -> sparse
-                              attention with fused linear read + sum)
+  hf_pool_keys               (key blocks of the chunk's 3 new frames, into
+                              the pooled-key cache)
+  hf_hybrid_forward_ex       (query pooling -> score/top-K with the cached
+                              key pools -> state prep -> sparse attention with
+                              fused linear read + sum)
 Inputs are synthetic (seeded Philox, see workloads.py) and resident in HBM.
-The step is captured once as a CUDA graph (its 5 kernels, no host work in
+The step is captured once as a CUDA graph (its 6 kernels, no host work in
 between) and replayed; L2 is flushed (256 MB write) before every timed
 replay, and each replay is timed with CUDA events on the launching stream.
 value = algorithmic FLOPs of the step / device time (effective TFLOP/s);
-us_per_latent_frame = time / 3.  A second, un-graphed loop records events
-between the kernels for the per-kernel breakdown and the attention kernel's
-roofline figure.  e2e streams chunks from pinned host memory through
+us_per_latent_frame = time / 3.  A second graph of the same step records
+events between its kernels (external event nodes) for the per-kernel
+breakdown and the attention kernel's roofline figure.  e2e streams chunks from pinned host memory through
 stream.HostStreamer (copies overlapped with compute).
 
 --impl reference times the CPU oracle (plain C, fp64) on the host cores on
@@ -94,8 +97,9 @@ def step_bytes(w, n_ev_tokens: int) -> dict:
     o = q
     ev = 2 * BH * n_ev_tokens * d * 2
     state = 2 * BH * (d * d + d) * 4
-    pool = q + BH * Nk * d * 2           # pooling reads Q and K of the window
-    return {"compulsory": q + kv + o + ev + state, "pool": pool, "absorb": ev + state}
+    pool_q = q                           # pooling the chunk's queries
+    pool_k = BH * w.chunk_frames * nf * d * 2   # pooling the new chunk's keys (the cache holds the rest)
+    return {"compulsory": q + kv + o + ev + state, "pool_q": pool_q, "pool_k": pool_k, "absorb": ev + state}
 
 
 class ClockSampler:
@@ -353,18 +357,23 @@ def run_hf(args):
     O = torch.empty_like(Q)
     idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(0)), dtype=torch.int32, device=dev)
     evict_slot = w.window(0)[0] % L.R                     # the oldest chunk's slots (contiguous)
+    chunk_slots = [f % L.R for f in w.chunk(0)]           # the slots the chunk's frames were written to
     n_ev = w.chunk_frames * w.tokens_per_frame
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def one_step(stream, events=None):
+        """absorb the evicted frames, pool the new chunk's key blocks, hybrid
+        forward with the other window frames' key pools from the cache."""
+        if events is not None:
+            events[0].record(stream)
         L.absorb_slots(evict_slot, w.chunk_frames, stream)
         if events is not None:
-            hb.hf_hybrid_forward_profiled(L.cfg, Q, L.Kc, L.Vc, L.ss, L.slot_map(), L.n_win(), L.S, L.z, O, idx,
-                                          L.ws, events, stream)
-        else:
-            L.forward(Q, O, idx, stream)
+            events[1].record(stream)
+        L.pool_slots(chunk_slots, stream)
+        L.forward(Q, O, idx, stream, events[2:] if events is not None else None)
 
     stream = torch.cuda.current_stream(dev)
+    L.forward(Q, O, idx, stream)                          # fills the key-pool cache for the window
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         one_step(stream)
@@ -373,7 +382,7 @@ def run_hf(args):
     fl = step_flops(w, idx.cpu().numpy(), n_ev)
     by = step_bytes(w, n_ev)
 
-    # ---- the step as one CUDA graph (5 kernels, no host work between them) ----
+    # ---- the step as one CUDA graph (6 kernels, no host work between them) ----
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(dev)
     with torch.cuda.stream(cap):
@@ -412,21 +421,25 @@ def run_hf(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # ---- per-kernel breakdown (events between the kernels, not graphed) ----
-    names = ["absorb", "pool", "score_topk", "state_prep", "attention"]
+    # ---- per-kernel breakdown: the same step captured with event records between
+    #      its kernels (external event nodes, so they time every replay) ----
+    names = ["absorb", "pool_keys", "pool", "score_topk", "state_prep", "attention"]
     times = {n: [] for n in names}
     n_prof = min(args.steps, 200)
-    pevs = []
-    for _ in range(n_prof):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        flush.zero_()
-        ev[0].record(stream)
-        one_step(stream, ev[1:6])
-        pevs.append(ev)
+    pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
+    for e in pev:                                         # create the CUDA events before the capture
+        e.record(stream)
     torch.cuda.synchronize()
-    for ev in pevs:
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=cap):
+        one_step(torch.cuda.current_stream(dev), pev)
+    torch.cuda.synchronize()
+    for _ in range(n_prof):
+        flush.zero_()
+        graph_ev.replay()
+        torch.cuda.synchronize()
         for i, n in enumerate(names):
-            times[n].append(ev[i].elapsed_time(ev[i + 1]))
+            times[n].append(pev[i].elapsed_time(pev[i + 1]))
 
     # warm-L2 timing of the graphed step, for context
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -474,14 +487,16 @@ def run_hf(args):
     for n in names:
         per_kernel[n]["share"] = per_kernel[n]["ms"] / tot_k
     per_kernel["absorb"]["GB_s"] = by["absorb"] / (per_kernel["absorb"]["ms"] * 1e-3) / 1e9
-    per_kernel["pool"]["GB_s"] = by["pool"] / (per_kernel["pool"]["ms"] * 1e-3) / 1e9
+    per_kernel["pool"]["GB_s"] = by["pool_q"] / (per_kernel["pool"]["ms"] * 1e-3) / 1e9
+    per_kernel["pool_keys"]["GB_s"] = by["pool_k"] / (per_kernel["pool_keys"]["ms"] * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "l2": "flushed (256 MB write) before every step",
-                   "timing": "CUDA events around each replay of the step's CUDA graph (absorb + hybrid "
-                             "forward, 5 kernels)", "parallelism": f"replicas x{ws}"},
+                   "timing": "CUDA events around each replay of the step's CUDA graph (absorb, key pooling of "
+                             "the new chunk, hybrid forward with cached key pools: 6 kernels)",
+                   "parallelism": f"replicas x{ws}"},
         "us_per_latent_frame": 1000 * ms / w.chunk_frames,
         "pct_bf16_peak": 100 * value / pk["bf16_tflops"],
         "warm_l2_ms_per_step": warm_ms,
@@ -491,7 +506,7 @@ def run_hf(args):
                      "achieved": attn_tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": attn_tf / pk["bf16_tflops"], "traffic": attention_traffic(),
                      "peak_source": pk["source"] + " burst", "peak_sustained": pk["bf16_tflops_sustained"]},
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 6 * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }

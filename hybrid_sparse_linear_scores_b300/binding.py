@@ -64,6 +64,9 @@ def lib():
                                             ctypes.POINTER(ctypes.c_void_p)], _I),
             "hf_hybrid_forward_noalloc": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P,
                                            ctypes.POINTER(ctypes.c_void_p), _P], _I),
+            "hf_hybrid_forward_ex": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_uint32,
+                                      ctypes.POINTER(ctypes.c_void_p)], _I),
+            "hf_pool_keys": ([cfgp, _P, _I, _P, _I, _P, _P], _I),
             "hf_get_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
             "hf_selftest_wait_timeout": ([_P, _I, _P], _I),
         }
@@ -184,6 +187,35 @@ def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, 
     _check(lib().hf_hybrid_forward_profiled(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
                                             sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
                                             _ptr(ws), st, ev), "hf_hybrid_forward_profiled")
+
+
+HF_FWD_CACHED_KEYS = 1
+
+
+def hf_pool_keys(cfg, Kc, slot_stride, slots, ws, stream=None):
+    """Pool the key blocks of the given ring slots into the workspace's cache."""
+    sl = _slots(list(slots))
+    _check(lib().hf_pool_keys(ctypes.byref(cfg), _ptr(Kc), int(slot_stride), sl and sl[0], len(list(slots)),
+                              _ptr(ws), _stream(stream)), "hf_pool_keys")
+
+
+def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, flags=0, events=None,
+                         stream=None):
+    """hf_hybrid_forward with flags (HF_FWD_CACHED_KEYS) and optional per-kernel
+    events (5 torch.cuda.Event objects, handled as in hf_hybrid_forward_profiled)."""
+    st = _stream(stream)
+    ev = None
+    if events is not None:
+        import torch
+        ts = torch.cuda.ExternalStream(st.value) if st.value else torch.cuda.current_stream()
+        for e in events:
+            if e is not None and not e.cuda_event:   # torch creates the CUDA event on its first record
+                e.record(ts)
+        ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
+    sm = _slots(slot_map)
+    _check(lib().hf_hybrid_forward_ex(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride), sm and sm[0],
+                                      int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out), _ptr(ws), st,
+                                      ctypes.c_uint32(int(flags)), ev), "hf_hybrid_forward_ex")
 
 
 def hf_hybrid_forward_noalloc(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, stream=None):

@@ -126,6 +126,16 @@ hf_status check_window(const hf_config* cfg, int32_t slot_stride, const int32_t*
     return HF_OK;
 }
 
+// Pool the chunk's queries and the keys of every frame of the window.
+PoolFrames window_frames(const SlotMap& sm, int n_win)
+{
+    PoolFrames pf;
+    for (int w = 0; w < HF_MAX_WINDOW_FRAMES; ++w) pf.slot[w] = w < n_win ? sm.s[w] : 0;
+    pf.n = n_win;
+    pf.with_q = 1;
+    return pf;
+}
+
 #define HF_CHECK_PTR(p)                                                                          \
     do {                                                                                         \
         if (!(p)) return fail(HF_ERR_INVALID_ARG, "%s is NULL", #p);                             \
@@ -273,8 +283,8 @@ hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_
     uint8_t* w = static_cast<uint8_t*>(ws);
     float* qp = reinterpret_cast<float*>(w + L.qp);
     float* kp = reinterpret_cast<float*>(w + L.kp);
-    HF_LAUNCH(launch_pool(Q, Kc, g, sm, qp, kp, stream), "pool launch");
-    HF_LAUNCH(launch_score_select(qp, kp, g, scores, nullptr, stream), "score launch");
+    HF_LAUNCH(launch_pool(Q, Kc, g, window_frames(sm, n_win), qp, kp, stream), "pool launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, stream), "score launch");
     return HF_OK;
 }
 
@@ -331,13 +341,14 @@ hf_status hf_linear_read(const hf_config* cfg, const uint16_t* Q, const float* S
     return HF_OK;
 }
 
-hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
-                                     int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
-                                     const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream,
-                                     void* const* events)
+hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                               int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
+                               const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags,
+                               void* const* events)
 {
     hf_status s = check_cfg(cfg);
     if (s != HF_OK) return s;
+    if (flags & ~(uint32_t)HF_FWD_CACHED_KEYS) return fail(HF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     HF_CHECK_PTR(Q);
     HF_CHECK_PTR(Kc);
     HF_CHECK_PTR(Vc);
@@ -357,13 +368,23 @@ hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, co
     uint16_t* smma = reinterpret_cast<uint16_t*>(w + L.smma);
     uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // inside a stream capture an event becomes an external record node, so that it
+    // also times the graph's replays
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    if (events && cudaStreamIsCapturing(st, &capturing) != cudaSuccess) capturing = cudaStreamCaptureStatusNone;
     auto mark = [&](int i) -> int {
-        return events && events[i] ? (int)cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : 0;
+        if (!events || !events[i]) return 0;
+        cudaEvent_t e = static_cast<cudaEvent_t>(events[i]);
+        return capturing == cudaStreamCaptureStatusActive
+                   ? (int)cudaEventRecordWithFlags(e, st, cudaEventRecordExternal)
+                   : (int)cudaEventRecord(e, st);
     };
+    PoolFrames pf = window_frames(sm, n_win);
+    if (flags & HF_FWD_CACHED_KEYS) pf.n = 0;   // the window's key blocks are already in the cache
     HF_LAUNCH(mark(0), "event record");
-    HF_LAUNCH(launch_pool(Q, Kc, g, sm, qp, kp, stream), "pool launch");
+    HF_LAUNCH(launch_pool(Q, Kc, g, pf, qp, kp, stream), "pool launch");
     HF_LAUNCH(mark(1), "event record");
-    HF_LAUNCH(launch_score_select(qp, kp, g, nullptr, idx, stream), "score/select launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, stream), "score/select launch");
     HF_LAUNCH(mark(2), "event record");
     HF_LAUNCH(launch_smma_prep(S, g, smma, stream), "state prep launch");
     HF_LAUNCH(mark(3), "event record");
@@ -373,12 +394,54 @@ hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, co
     return HF_OK;
 }
 
+hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                                     int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
+                                     const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream,
+                                     void* const* events)
+{
+    return hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u,
+                                events);
+}
+
 hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
                             int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
                             const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream)
 {
-    return hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream,
-                                      nullptr);
+    return hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u,
+                                nullptr);
+}
+
+hf_status hf_pool_keys(const hf_config* cfg, const uint16_t* Kc, int32_t slot_stride, const int32_t* slots,
+                       int32_t n_slots, void* ws, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(Kc);
+    HF_CHECK_PTR(ws);
+    if (n_slots < 0 || n_slots > cfg->window_frames)
+        return fail(HF_ERR_INVALID_ARG, "n_slots %d not in [0, window_frames %d]", n_slots, cfg->window_frames);
+    if (slot_stride < cfg->tokens_per_frame)
+        return fail(HF_ERR_INVALID_ARG, "slot_stride %d < tokens_per_frame %d", slot_stride, cfg->tokens_per_frame);
+    if (n_slots > 0 && !slots) return fail(HF_ERR_INVALID_ARG, "slots is NULL");
+    PoolFrames pf;
+    uint64_t used = 0;
+    for (int i = 0; i < HF_MAX_WINDOW_FRAMES; ++i) pf.slot[i] = 0;
+    for (int i = 0; i < n_slots; ++i) {
+        const int sl = slots[i];
+        if (sl < 0 || sl >= cfg->window_frames)
+            return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d outside [0, %d)", i, sl, cfg->window_frames);
+        if (used & (1ull << sl)) return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d given twice", i, sl);
+        used |= 1ull << sl;
+        pf.slot[i] = sl;
+    }
+    pf.n = n_slots;
+    pf.with_q = 0;
+    if (n_slots == 0) return HF_OK;
+    const Geom g = make_geom(cfg, cfg->chunk_frames, slot_stride);
+    const WsLayout L = ws_layout(cfg);
+    float* kp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.kp);
+    HF_LAUNCH(launch_pool(nullptr, Kc, g, pf, nullptr, kp, stream), "key pool launch");
+    return HF_OK;
 }
 
 hf_status hf_get_device_status(void* ws, void* stream, int32_t* site)

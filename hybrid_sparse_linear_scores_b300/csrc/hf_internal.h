@@ -40,6 +40,14 @@ struct SlotMap {
     int32_t s[HF_MAX_WINDOW_FRAMES];
 };
 
+// What a pooling launch covers: the chunk's query blocks (with_q) and the
+// key blocks of the ring slots slot[0..n).
+struct PoolFrames {
+    int32_t slot[HF_MAX_WINDOW_FRAMES];
+    int32_t n;
+    int32_t with_q;
+};
+
 // Geometry of one call, derived and validated on the host.
 struct Geom {
     int32_t BH;          // batch * heads
@@ -62,17 +70,17 @@ struct Geom {
 struct WsLayout {
     size_t status;   // 256 B: uint32 [0] code, [1] site
     size_t qp;       // fp32 [BH][nQB][d]
-    size_t kp;       // fp32 [BH][nKB_max][d]
+    size_t kp;       // fp32 [BH][W slots][d][bpf]: pooled keys of every ring slot (kept between calls)
     size_t idx;      // int32 [BH][nQB][K_max]
     size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout)
     size_t total;
 };
 
 // ---- launchers (return cudaError_t as int) --------------------------------
-int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const SlotMap& sm, float* qp, float* kp,
+int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* qp, float* kpc,
                 void* stream);
-int launch_score_select(const float* qp, const float* kp, const Geom& g, float* scores, int32_t* idx,
-                        void* stream);
+int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
+                        int32_t* idx, void* stream);
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
 int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
                 const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,

@@ -21,83 +21,99 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // Pooling: one task = one block (beta tokens of one frame) of Q (chunk) or
-// K (window, through the ring).  D/8 threads per task, 8 channels each
-// (one 16-byte load per token); sequential float32 sums.
+// of K (frames of the ring named by `frames`).  D/8 threads per task, each
+// owning 8 channels: a thread copies its 16-byte slice of every row of the
+// block into shared memory with cp.async (all rows in flight at once, one
+// memory round trip), then adds them in token order (sequential float32
+// sums).  No data is shared between threads, so no barrier is needed.
+// Outputs: qp [BH][nqb][D] (row-major); key pools go to the per-slot cache
+// kpc [BH][W slots][D][bpf] (channel-major inside a slot, so that the score
+// kernel reads one block's channels with one thread per block).
 // ---------------------------------------------------------------------------
+constexpr int kPoolThreads = 64;
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gsrc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <int D>
-__global__ void __launch_bounds__(256) pool_kernel(const uint16_t* __restrict__ Q, const uint16_t* __restrict__ Kc,
-                                                   Geom g, SlotMap sm, float* __restrict__ qp,
-                                                   float* __restrict__ kp)
+__global__ void __launch_bounds__(kPoolThreads) pool_kernel(const uint16_t* __restrict__ Q,
+                                                            const uint16_t* __restrict__ Kc, Geom g, PoolFrames pf,
+                                                            float* __restrict__ qp, float* __restrict__ kpc)
 {
     constexpr int TPB = D / 8;
-    constexpr int TASKS = 256 / TPB;
+    constexpr int TASKS = kPoolThreads / TPB;
+    constexpr int ROW = D / 8;   // uint4 per token row
+    extern __shared__ __align__(16) uint4 stage[];   // [beta rows][kPoolThreads]
     const int task = blockIdx.x * TASKS + threadIdx.x / TPB;
     const int part = threadIdx.x % TPB;
-    const int per_head = g.nqb + g.nkb;
+    const int nq = pf.with_q ? g.nqb : 0;
+    const int per_head = nq + pf.n * g.bpf;
     if (task >= g.BH * per_head) return;
     const int bh = task / per_head;
     const int b = task - bh * per_head;
 
     const uint16_t* src;
-    float* dst;
     int j;
-    if (b < g.nqb) {
+    bool is_q;
+    int slot = 0;
+    if (b < nq) {
         const int c = b / g.bpf;
         j = b - c * g.bpf;
         src = Q + ((size_t)bh * g.C * g.nf + (size_t)c * g.nf + (size_t)j * g.beta) * D;
-        dst = qp + ((size_t)bh * g.nqb + b) * D;
+        is_q = true;
     } else {
-        const int kb = b - g.nqb;
-        const int w = kb / g.bpf;
-        j = kb - w * g.bpf;
-        const int slot = sm.s[w];
+        const int f = (b - nq) / g.bpf;
+        j = (b - nq) - f * g.bpf;
+        slot = pf.slot[f];
         src = Kc + (((size_t)bh * g.W + slot) * g.slot_stride + (size_t)j * g.beta) * D;
-        dst = kp + ((size_t)bh * g.nkb + kb) * D;
+        is_q = false;
     }
     const int n = min(g.beta, g.nf - j * g.beta);
     const uint4* p = reinterpret_cast<const uint4*>(src) + part;
-    constexpr int ROW = D / 8;   // uint4 per token row
+    for (int r = 0; r < n; ++r) cp_async16(&stage[r * kPoolThreads + threadIdx.x], p + (size_t)r * ROW);
+    cp_async_wait_all();
 
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-
-    for (int t0 = 0; t0 < n; t0 += 8) {
-        uint4 v[8];
+    for (int r = 0; r < n; ++r) {
+        const uint4 v = stage[r * kPoolThreads + threadIdx.x];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (t0 + u < n) v[u] = __ldg(p + (size_t)(t0 + u) * ROW);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (t0 + u < n) {
-                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(w4[i] << 16));
-                    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(w4[i] & 0xFFFF0000u));
-                }
-            }
+        for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(w4[i] << 16));
+            acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(w4[i] & 0xFFFF0000u));
         }
     }
     const float fn = static_cast<float>(n);
-    float4 o0, o1;
-    o0.x = __fdiv_rn(acc[0], fn);
-    o0.y = __fdiv_rn(acc[1], fn);
-    o0.z = __fdiv_rn(acc[2], fn);
-    o0.w = __fdiv_rn(acc[3], fn);
-    o1.x = __fdiv_rn(acc[4], fn);
-    o1.y = __fdiv_rn(acc[5], fn);
-    o1.z = __fdiv_rn(acc[6], fn);
-    o1.w = __fdiv_rn(acc[7], fn);
-    reinterpret_cast<float4*>(dst)[2 * part] = o0;
-    reinterpret_cast<float4*>(dst)[2 * part + 1] = o1;
+    if (is_q) {
+        float* dst = qp + ((size_t)bh * g.nqb + b) * D + 8 * part;
+        reinterpret_cast<float4*>(dst)[0] =
+            make_float4(__fdiv_rn(acc[0], fn), __fdiv_rn(acc[1], fn), __fdiv_rn(acc[2], fn), __fdiv_rn(acc[3], fn));
+        reinterpret_cast<float4*>(dst)[1] =
+            make_float4(__fdiv_rn(acc[4], fn), __fdiv_rn(acc[5], fn), __fdiv_rn(acc[6], fn), __fdiv_rn(acc[7], fn));
+    } else {
+        float* dst = kpc + (((size_t)bh * g.W + slot) * D + 8 * part) * g.bpf + j;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[(size_t)i * g.bpf] = __fdiv_rn(acc[i], fn);
+    }
 }
 
 // ---------------------------------------------------------------------------
-// Warp top-K: radix select (4 passes of 8 bits) on order-preserving uint32
-// keys of the float scores finds the K-th largest key T; keys > T are all
-// selected, keys == T are taken in ascending block order until K.  Output is
-// written in ascending block order with ballots.  `s` is in shared memory.
+// Warp top-K.  Scores are mapped to order-preserving uint32 keys (in place
+// over `s`).  The K-th largest key T is found bit by bit from the top: T is
+// the largest value with at least K keys >= T (32 warp-wide counts).  Keys
+// > T are all selected, keys == T are taken in ascending block order until
+// K.  The winners are written in ascending block order with ballots.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(float f)
 {
@@ -105,67 +121,46 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ void warp_topk(const float* s, int n, int K, int32_t* __restrict__ out, uint32_t* hist)
+__device__ void warp_topk(float* s, int n, int K, int32_t* __restrict__ out)
 {
     const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0, pmask = 0;
-    int remaining = K;   // how many of the K still to place at or below the current prefix
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    uint32_t* keys = reinterpret_cast<uint32_t*>(s);
+    for (int e = lane; e < n; e += 32) keys[e] = order_key(s[e]);
+    __syncwarp();
+    uint32_t T = 0;
+    if (n <= 256) {   // up to 8 keys per lane, kept in registers
+        uint32_t kr[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
-        __syncwarp();
-        for (int e = lane; e < n; e += 32) {
-            const uint32_t key = order_key(s[e]);
-            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-        }
-        __syncwarp();
-        // Lane l owns digits [8l, 8l+8).  Count keys with a larger digit.
-        uint32_t loc[8];
-        uint32_t lsum = 0;
+        for (int i = 0; i < 8; ++i) kr[i] = lane + 32 * i < n ? keys[lane + 32 * i] : 0u;
+        const int nmine = n > lane ? (n - lane + 31) / 32 : 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = T | (1u << bit);
+            int cnt = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            loc[i] = hist[lane * 8 + i];
-            lsum += loc[i];
+            for (int i = 0; i < 8; ++i) cnt += (i < nmine && kr[i] >= cand) ? 1 : 0;
+            cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+            if (cnt >= K) T = cand;
         }
-        // suffix sum over lanes (higher lanes own larger digits)
-        uint32_t sfx = lsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, sfx, o);
-            if (lane + o < 32) sfx += v;
+    } else {
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = T | (1u << bit);
+            int cnt = 0;
+            for (int e = lane; e < n; e += 32) cnt += keys[e] >= cand ? 1 : 0;
+            cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+            if (cnt >= K) T = cand;
         }
-        const uint32_t above = sfx - lsum;   // keys with digit in lanes > lane
-        // the digit holding the remaining-th largest lies in the lane with
-        // above < remaining <= above + lsum
-        const bool mine = (above < (uint32_t)remaining) && ((uint32_t)remaining <= above + lsum);
-        const uint32_t ball = __ballot_sync(0xFFFFFFFFu, mine);
-        const int owner = __ffs(ball) - 1;
-        uint32_t digit = 0, gt = 0;
-        if (lane == owner) {
-            uint32_t acc = above;
-            for (int i = 7; i >= 0; --i) {
-                if ((uint32_t)remaining <= acc + loc[i]) {
-                    digit = lane * 8 + i;
-                    gt = acc;
-                    break;
-                }
-                acc += loc[i];
-            }
-        }
-        digit = __shfl_sync(0xFFFFFFFFu, digit, owner);
-        gt = __shfl_sync(0xFFFFFFFFu, gt, owner);
-        remaining -= (int)gt;
-        prefix |= digit << shift;
-        pmask |= 255u << shift;
-        __syncwarp();
     }
-    // prefix == T; `remaining` keys equal to T are still needed.
+    // keys > T: all selected; keys == T: the first (K - #greater) in block order
+    int gt_total = 0;
+    for (int e = lane; e < n; e += 32) gt_total += keys[e] > T ? 1 : 0;
+    gt_total = __reduce_add_sync(0xFFFFFFFFu, gt_total);
+    const int remaining = K - gt_total;
     int pos = 0, eq_taken = 0;
     for (int base = 0; base < n; base += 32) {
         const int e = base + lane;
-        const uint32_t key = e < n ? order_key(s[e]) : 0u;
-        const bool gt = e < n && key > prefix;
-        const bool eq = e < n && key == prefix;
+        const uint32_t key = e < n ? keys[e] : 0u;
+        const bool gt = e < n && key > T;
+        const bool eq = e < n && key == T;
         const uint32_t eqb = __ballot_sync(0xFFFFFFFFu, eq);
         const int eq_rank = eq_taken + __popc(eqb & ((1u << lane) - 1u));
         const bool sel = gt || (eq && eq_rank < remaining);
@@ -178,31 +173,31 @@ __device__ void warp_topk(const float* s, int n, int K, int32_t* __restrict__ ou
 
 // ---------------------------------------------------------------------------
 // Scores (+ optional selection) for a group of QG query blocks of one head.
-// Pooled keys are staged in shared memory in chunks of 128 rows with a row
-// pitch of D+1 floats (conflict-free column reads).
+// One thread per key block: it copies the block's D pooled channels from the
+// slot cache into its own column of shared memory (cp.async, all in flight),
+// then runs the QG dot products as separate fixed-order fma chains with the
+// query pools broadcast from shared memory.  One warp per query block then
+// selects its top K.
 // ---------------------------------------------------------------------------
 constexpr int QG = 8;
-constexpr int KCH = 128;
 
 template <int D>
 struct ScoreSmem {
-    static constexpr int KP = KCH * (D + 1);   // floats
     static constexpr int QP = QG * D;          // floats
     static constexpr int S = QG * HF_MAX_KEY_BLOCKS;
-    static constexpr int HIST = 8 * 256;       // uint32, one histogram per warp
-    static constexpr size_t bytes = sizeof(float) * (KP + QP + S) + sizeof(uint32_t) * HIST;
+    static constexpr int KS = D * 256;         // [D][256]: the key blocks of one pass, one column per thread
+    static constexpr size_t bytes = sizeof(float) * (QP + S + KS);
 };
 
 template <int D, bool WRITE_SCORES, bool SELECT>
-__global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qp, const float* __restrict__ kp,
-                                                           Geom g, float* __restrict__ scores,
+__global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qp, const float* __restrict__ kpc,
+                                                           Geom g, SlotMap sm, float* __restrict__ scores,
                                                            int32_t* __restrict__ idx)
 {
     extern __shared__ __align__(16) float smf[];
-    float* kps = smf;
-    float* qps = kps + ScoreSmem<D>::KP;
+    float* qps = smf;
     float* ss = qps + ScoreSmem<D>::QP;
-    uint32_t* hist = reinterpret_cast<uint32_t*>(ss + ScoreSmem<D>::S);
+    float* ks = ss + ScoreSmem<D>::S;
 
     const int groups = (g.nqb + QG - 1) / QG;
     const int bh = blockIdx.x / groups;
@@ -210,46 +205,54 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
     const int nq = min(QG, g.nqb - qb0);
     const int tid = threadIdx.x;
 
-    for (int i = tid; i < QG * D; i += 256) {
-        const int q = i / D;
-        qps[i] = q < nq ? qp[((size_t)bh * g.nqb + qb0 + q) * D + (i - q * D)] : 0.0f;
+    for (int i = tid; i < QG * D / 4; i += 256) {
+        const int q = (4 * i) / D;
+        reinterpret_cast<float4*>(qps)[i] =
+            q < nq ? reinterpret_cast<const float4*>(qp + ((size_t)bh * g.nqb + qb0) * D)[i] : make_float4(0, 0, 0, 0);
     }
-    const float* kph = kp + (size_t)bh * g.nkb * D;
-    for (int base = 0; base < g.nkb; base += KCH) {
-        const int rows = min(KCH, g.nkb - base);
-        __syncthreads();
-        for (int i = tid; i < rows * D; i += 256) {
-            const int r = i / D;
-            kps[r * (D + 1) + (i - r * D)] = kph[(size_t)base * D + i];
-        }
-        __syncthreads();
-        const int r = tid % KCH;
-        const int qh = tid / KCH;   // 0 or 1: query rows qh*4 .. qh*4+3
-        if (r < rows) {
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const float* krow = kps + r * (D + 1);
-            const float* q0 = qps + (qh * 4) * D;
+    __syncthreads();
+    for (int kb = tid; kb < g.nkb; kb += 256) {
+        const int w = kb / g.bpf;
+        const int j = kb - w * g.bpf;
+        const float* kcol = kpc + ((size_t)bh * g.W + sm.s[w]) * D * g.bpf + j;
+        // this thread's column of the staging area: all D loads in flight at once
+#pragma unroll 16
+        for (int c = 0; c < D; ++c)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(
+                             __cvta_generic_to_shared(ks + c * 256 + tid))),
+                         "l"(kcol + (size_t)c * g.bpf)
+                         : "memory");
+        cp_async_wait_all();
+        float acc[QG];
+#pragma unroll
+        for (int q = 0; q < QG; ++q) acc[q] = 0.0f;
 #pragma unroll 4
-            for (int c = 0; c < D; ++c) {
-                const float kv = krow[c];
+        for (int c = 0; c < D; c += 4) {
+            const float k0 = ks[c * 256 + tid], k1 = ks[(c + 1) * 256 + tid];
+            const float k2 = ks[(c + 2) * 256 + tid], k3 = ks[(c + 3) * 256 + tid];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = __fmaf_rn(q0[i * D + c], kv, acc[i]);
+            for (int q = 0; q < QG; ++q) {
+                const float4 q4 = *reinterpret_cast<const float4*>(qps + q * D + c);
+                acc[q] = __fmaf_rn(q4.x, k0, acc[q]);
+                acc[q] = __fmaf_rn(q4.y, k1, acc[q]);
+                acc[q] = __fmaf_rn(q4.z, k2, acc[q]);
+                acc[q] = __fmaf_rn(q4.w, k3, acc[q]);
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ss[(qh * 4 + i) * HF_MAX_KEY_BLOCKS + base + r] = acc[i] + 0.0f;
         }
+#pragma unroll
+        for (int q = 0; q < QG; ++q) ss[q * HF_MAX_KEY_BLOCKS + kb] = acc[q] + 0.0f;
     }
     __syncthreads();
     if (WRITE_SCORES) {
         for (int q = 0; q < nq; ++q)
             for (int kb = tid; kb < g.nkb; kb += 256)
                 scores[((size_t)bh * g.nqb + qb0 + q) * g.nkb + kb] = ss[q * HF_MAX_KEY_BLOCKS + kb];
+        if (SELECT) __syncthreads();   // the selection overwrites the rows with keys
     }
     if (SELECT) {
         const int warp = tid / 32;
         if (warp < nq)
-            warp_topk(ss + warp * HF_MAX_KEY_BLOCKS, g.nkb, g.k_eff,
-                      idx + ((size_t)bh * g.nqb + qb0 + warp) * g.k_eff, hist + warp * 256);
+            warp_topk(ss + warp * HF_MAX_KEY_BLOCKS, g.nkb, g.k_eff, idx + ((size_t)bh * g.nqb + qb0 + warp) * g.k_eff);
     }
 }
 
@@ -263,11 +266,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ sco
     const long row = (long)blockIdx.x * 8 + warp;
     const long rows = (long)g.BH * g.nqb;
     float* s = smf + warp * HF_MAX_KEY_BLOCKS;
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smf + 8 * HF_MAX_KEY_BLOCKS) + warp * 256;
     if (row >= rows) return;
     for (int e = lane; e < g.nkb; e += 32) s[e] = scores[row * g.nkb + e] + 0.0f;
     __syncwarp();
-    warp_topk(s, g.nkb, g.k_eff, idx + row * g.k_eff, hist);
+    warp_topk(s, g.nkb, g.k_eff, idx + row * g.k_eff);
 }
 
 template <typename K>
@@ -278,51 +280,57 @@ cudaError_t set_smem(K kernel, size_t bytes)
 
 }  // namespace
 
-int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const SlotMap& sm, float* qp, float* kp,
+int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* qp, float* kpc,
                 void* stream)
 {
-    const long tasks = (long)g.BH * (g.nqb + g.nkb);
+    const long tasks = (long)g.BH * ((pf.with_q ? g.nqb : 0) + pf.n * g.bpf);
+    if (tasks == 0) return 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t smem = (size_t)g.beta * kPoolThreads * 16;   // one 16-byte slice per row and thread
     if (g.d == 128) {
-        const long grid = (tasks + 15) / 16;
-        pool_kernel<128><<<(unsigned)grid, 256, 0, st>>>(Q, Kc, g, sm, qp, kp);
+        cudaError_t e = set_smem(pool_kernel<128>, smem);
+        if (e != cudaSuccess) return (int)e;
+        const long grid = (tasks + kPoolThreads / 16 - 1) / (kPoolThreads / 16);
+        pool_kernel<128><<<(unsigned)grid, kPoolThreads, smem, st>>>(Q, Kc, g, pf, qp, kpc);
     } else {
-        const long grid = (tasks + 31) / 32;
-        pool_kernel<64><<<(unsigned)grid, 256, 0, st>>>(Q, Kc, g, sm, qp, kp);
+        cudaError_t e = set_smem(pool_kernel<64>, smem);
+        if (e != cudaSuccess) return (int)e;
+        const long grid = (tasks + kPoolThreads / 8 - 1) / (kPoolThreads / 8);
+        pool_kernel<64><<<(unsigned)grid, kPoolThreads, smem, st>>>(Q, Kc, g, pf, qp, kpc);
     }
     return (int)cudaGetLastError();
 }
 
 template <int D, bool W, bool S>
-static int launch_score_t(const float* qp, const float* kp, const Geom& g, float* scores, int32_t* idx,
-                          cudaStream_t st)
+static int launch_score_t(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
+                          int32_t* idx, cudaStream_t st)
 {
     auto k = score_select_kernel<D, W, S>;
     cudaError_t e = set_smem(k, ScoreSmem<D>::bytes);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + QG - 1) / QG;
-    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kp, g, scores, idx);
+    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kpc, g, sm, scores, idx);
     return (int)cudaGetLastError();
 }
 
-int launch_score_select(const float* qp, const float* kp, const Geom& g, float* scores, int32_t* idx,
-                        void* stream)
+int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
+                        int32_t* idx, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool w = scores != nullptr, s = idx != nullptr;
     if (g.d == 128) {
-        if (w && s) return launch_score_t<128, true, true>(qp, kp, g, scores, idx, st);
-        if (w) return launch_score_t<128, true, false>(qp, kp, g, scores, idx, st);
-        return launch_score_t<128, false, true>(qp, kp, g, scores, idx, st);
+        if (w && s) return launch_score_t<128, true, true>(qp, kpc, g, sm, scores, idx, st);
+        if (w) return launch_score_t<128, true, false>(qp, kpc, g, sm, scores, idx, st);
+        return launch_score_t<128, false, true>(qp, kpc, g, sm, scores, idx, st);
     }
-    if (w && s) return launch_score_t<64, true, true>(qp, kp, g, scores, idx, st);
-    if (w) return launch_score_t<64, true, false>(qp, kp, g, scores, idx, st);
-    return launch_score_t<64, false, true>(qp, kp, g, scores, idx, st);
+    if (w && s) return launch_score_t<64, true, true>(qp, kpc, g, sm, scores, idx, st);
+    if (w) return launch_score_t<64, true, false>(qp, kpc, g, sm, scores, idx, st);
+    return launch_score_t<64, false, true>(qp, kpc, g, sm, scores, idx, st);
 }
 
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream)
 {
-    const size_t bytes = sizeof(float) * 8 * HF_MAX_KEY_BLOCKS + sizeof(uint32_t) * 8 * 256;
+    const size_t bytes = sizeof(float) * 8 * HF_MAX_KEY_BLOCKS;
     cudaError_t e = set_smem(topk_kernel, bytes);
     if (e != cudaSuccess) return (int)e;
     const long rows = (long)g.BH * g.nqb;

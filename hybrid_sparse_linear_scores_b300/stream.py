@@ -46,6 +46,8 @@ class HybridAttentionLayer:
         self.z = torch.zeros((self.BH, self.d), dtype=torch.float32, device=self.device)
         self.ws = torch.zeros(hb.hf_workspace_size(self.cfg), dtype=torch.uint8, device=self.device)
         self.frames = 0
+        # ring slots whose pooled key blocks are in the workspace's cache (host bookkeeping)
+        self.pooled: set[int] = set()
 
     # ---- window bookkeeping (host) ----
     def n_win(self) -> int:
@@ -88,21 +90,42 @@ class HybridAttentionLayer:
         """Ring slots of the next chunk's frames."""
         return [(self.frames + c) % self.R for c in range(self.C)]
 
-    def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor):
-        """K_new, V_new: [BH, C, N_f, d] bf16 for the next C frames."""
-        for c, slot in enumerate(self.chunk_slots()):
+    def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor, stream=None):
+        """K_new, V_new: [BH, C, N_f, d] bf16 for the next C frames.  The
+        chunk's key blocks are pooled into the cache right after the copy."""
+        slots = self.chunk_slots()
+        for c, slot in enumerate(slots):
             self.Kc[:, slot, :self.nf].copy_(K_new[:, c])
             self.Vc[:, slot, :self.nf].copy_(V_new[:, c])
+        self.pool_slots(slots, stream)
         self.frames += self.C
 
-    def forward(self, Q: torch.Tensor, O: torch.Tensor, idx_out: torch.Tensor | None = None, stream=None):
-        """Q, O: [BH, C*N_f, d] bf16.  idx_out: optional int32 [BH, nQB, K_eff]."""
-        hb.hf_hybrid_forward(self.cfg, Q, self.Kc, self.Vc, self.ss, self.slot_map(), self.n_win(), self.S, self.z,
-                             O, idx_out, self.ws, stream)
+    def pool_slots(self, slots, stream=None):
+        """Pool the key blocks of freshly written ring slots into the cache."""
+        hb.hf_pool_keys(self.cfg, self.Kc, self.ss, list(slots), self.ws, stream)
+        self.pooled.update(slots)
+
+    def invalidate_key_cache(self, slots=None):
+        """Forget cached key pools (all, or of `slots`) after writing Kc directly."""
+        if slots is None:
+            self.pooled.clear()
+        else:
+            self.pooled.difference_update(slots)
+
+    def forward(self, Q: torch.Tensor, O: torch.Tensor, idx_out: torch.Tensor | None = None, stream=None,
+                events=None):
+        """Q, O: [BH, C*N_f, d] bf16.  idx_out: optional int32 [BH, nQB, K_eff].
+        Uses the cached key pools when every window slot is in the cache;
+        otherwise pools the whole window (which fills the cache)."""
+        sm = self.slot_map()
+        cached = all(sl in self.pooled for sl in sm)
+        hb.hf_hybrid_forward_ex(self.cfg, Q, self.Kc, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O, idx_out,
+                                self.ws, hb.HF_FWD_CACHED_KEYS if cached else 0, events, stream)
+        self.pooled.update(sm)
 
     def step(self, Q, K_new, V_new, O, idx_out=None, stream=None):
         self.absorb_evicted(stream)
-        self.write_chunk(K_new, V_new)
+        self.write_chunk(K_new, V_new, stream)
         self.forward(Q, O, idx_out, stream)
 
     # ---- checkpoint / resume ----
@@ -117,6 +140,7 @@ class HybridAttentionLayer:
         self.S.copy_(sd["S"])
         self.z.copy_(sd["z"])
         self.frames = int(sd["frames"])
+        self.invalidate_key_cache()   # the next forward re-pools the window
 
     def check_device_status(self, stream=None):
         rc, site = hb.hf_get_device_status(self.ws, stream)
@@ -182,6 +206,7 @@ class HostStreamer:
             L.absorb_slots(run[0], len(run), self.cs)
         self.ev_absorb.record(self.cs)
         self.cs.wait_event(self.ev_h2d[b])
+        L.pool_slots(slots, self.cs)                  # the chunk's key blocks, once they landed
         self.cs.wait_event(self.ev_d2h[b])            # Od[b] has been read back
         L.forward(self.Qd[b], self.Od[b], None, self.cs)
         self.ev_fwd[b].record(self.cs)

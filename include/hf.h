@@ -104,7 +104,9 @@ HF_API const char *hf_last_error(void);
  * `cfg` (sized for a full window of cfg->window_frames frames).  The same
  * workspace may be reused by every call on one stream; calls that run
  * concurrently need separate workspaces.  It must be zeroed once before
- * first use (its first 256 bytes are the device status word). */
+ * first use (its first 256 bytes are the device status word).  It also holds
+ * the pooled-key cache of the layer's ring (see hf_pool_keys): one workspace
+ * per ring. */
 HF_API hf_status hf_workspace_size(const hf_config *cfg, size_t *bytes /* host */);
 
 /* S = 0, z = 0 (the empty state). */
@@ -178,11 +180,43 @@ HF_API hf_status hf_hybrid_forward(const hf_config *cfg, const uint16_t *Q, cons
                             const float *S, const float *z, uint16_t *O, int32_t *idx_out,
                             void *ws, void *stream);
 
+/* Key-block pooling for the pooled-key cache (English technical summary,
+ * section 2.A.2: the block importance scores use pooled key blocks).  The
+ * workspace keeps the pooled keys of every ring slot, fp32 [b, H, W, d, bpf]
+ * (W = cfg->window_frames slots), between calls; a frame's key blocks do not
+ * change while it stays in the window, so they need to be pooled only once,
+ * when the frame is written into its slot.  This call pools the key blocks
+ * of the ring slots slots[0..n_slots) (host array of distinct slots in
+ * [0, W)) of Kc (bf16 [b, H, W, slot_stride, d]) into that cache.  The
+ * arithmetic is that of hf_block_scores, so the cached values are identical
+ * to the ones hf_hybrid_forward recomputes.  n_slots = 0 is a no-op. */
+HF_API hf_status hf_pool_keys(const hf_config *cfg, const uint16_t *Kc, int32_t slot_stride,
+                              const int32_t *slots /* host */, int32_t n_slots, void *ws, void *stream);
+
+/* Flags of hf_hybrid_forward_ex. */
+#define HF_FWD_CACHED_KEYS 1u  /* take the window's pooled keys from the cache
+                                  (every slot of the window pooled by hf_pool_keys,
+                                  or by an earlier forward, since it was last written);
+                                  only the chunk's queries are pooled */
+
+/* hf_hybrid_forward with options: `flags` (HF_FWD_CACHED_KEYS or 0) and
+ * per-kernel timing, `events` as in hf_hybrid_forward_profiled (may be NULL).
+ * Without HF_FWD_CACHED_KEYS every call pools the keys of the whole window
+ * (and leaves them in the cache). */
+HF_API hf_status hf_hybrid_forward_ex(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
+                                      const uint16_t *Vc, int32_t slot_stride,
+                                      const int32_t *slot_map /* host */, int32_t n_win,
+                                      const float *S, const float *z, uint16_t *O, int32_t *idx_out,
+                                      void *ws, void *stream, uint32_t flags,
+                                      void *const *events /* host, 5 entries, or NULL */);
+
 /* hf_hybrid_forward with per-kernel timing: events[0..4] (cudaEvent_t
  * handles created by the caller, or NULL for none) are recorded on `stream`
  * before the pooling kernel, before the score/select kernel, before the state
  * preparation kernel, before the attention kernel and after it.  The results
- * are identical to hf_hybrid_forward. */
+ * are identical to hf_hybrid_forward.  When `stream` is being captured into
+ * a CUDA graph the events are captured as external event records, so they
+ * time every replay of the graph. */
 HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
                                             const uint16_t *Vc, int32_t slot_stride,
                                             const int32_t *slot_map /* host */, int32_t n_win,

@@ -96,6 +96,39 @@ def test_sweep_sampled_rows(w, cuda_device):
     compare(O[heads][:, rows], ref["O"], what=w.name)
 
 
+@pytest.mark.parametrize("name", ["d128_b64_ragged8", "d128_b128_ragged44", "d128_b32_ragged4", "d64_b64"])
+def test_cached_key_pools_bit_identical(name, cuda_device):
+    """hf_pool_keys + hf_hybrid_forward_ex(HF_FWD_CACHED_KEYS) gives the same
+    indices and output bits as pooling the whole window in the forward, with
+    the ring slots pooled in an order different from the window's."""
+    w = SMALL[name]
+    st = Step(w, 0, cuda_device)
+    L = st.layer
+    O_ref, idx_ref = st.run_forward()                       # pools every window frame
+    # wipe the cache, then pool the window's slots one call per slot, newest first
+    L.ws[1024:].zero_()
+    L.invalidate_key_cache()
+    for sl in reversed(L.slot_map()):
+        L.pool_slots([sl])
+    O = torch.empty_like(st.Q)
+    idx = torch.empty_like(idx_ref)
+    hb.hf_hybrid_forward_ex(L.cfg, st.Q, L.Kc, L.Vc, L.ss, L.slot_map(), L.n_win(), L.S, L.z, O, idx, L.ws,
+                            hb.HF_FWD_CACHED_KEYS)
+    torch.cuda.synchronize()
+    L.check_device_status()
+    assert torch.equal(idx, idx_ref)
+    assert torch.equal(O.view(torch.int16), O_ref.view(torch.int16))
+
+
+def test_pool_keys_rejects_bad_slots(cuda_device):
+    w = SMALL["d128_b64_ragged8"]
+    L = HybridAttentionLayer(config_of(w, 0), cuda_device)
+    for slots in ([w.window_frames], [-1], [0, 0]):
+        with pytest.raises(hb.HFError) as e:
+            hb.hf_pool_keys(L.cfg, L.Kc, L.ss, slots, L.ws)
+        assert e.value.code == 1
+
+
 def test_standalone_entry_points(cuda_device):
     """hf_block_scores, hf_topk_blocks, hf_sparse_swa_attn, hf_linear_read,
     hf_absorb_evicted each against the matching oracle step."""
