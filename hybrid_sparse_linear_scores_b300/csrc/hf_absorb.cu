@@ -10,7 +10,7 @@
 // phi(k) enters the MMA as a bf16 pair hi + lo (hi = rn(phi), lo =
 // rn(phi - hi)), two MMAs into one fp32 accumulator, so S keeps ~16 bits
 // more than a bf16 operand would give; z is summed in fp32 on CUDA cores.
-// The tensor-core accumulator only ever holds one 128-token tile: two TMEM
+// The tensor-core accumulator only ever holds one 64-token tile: two TMEM
 // accumulators alternate, and the epilogue warps fold each finished tile
 // into fp32 registers with round-to-nearest adds while the next tile is
 // multiplied, so long absorbs do not accumulate the tensor core's internal
@@ -39,26 +39,28 @@ namespace {
 
 template <int D>
 struct AbsCfg {
-    static constexpr int TT = 128;                   // tokens per tile (MMA K extent per tile)
-    static constexpr int NS = 2;                     // stages
-    static constexpr int CHUNK = TT * 128;           // one 64-column chunk of a tile: 16 KB
+    static constexpr int TT = 64;                    // tokens per tile (MMA K extent per tile)
+    static constexpr int NS = 4;                     // stages
+    static constexpr int CHUNK = TT * 128;           // one 64-column chunk of a tile: 8 KB
     static constexpr int OFF_K = 0;                  // 2 chunks (chunk 1 zero when D = 64)
     static constexpr int OFF_LO = 2 * CHUNK;         // 2 chunks
     static constexpr int OFF_V = 4 * CHUNK;          // D/64 chunks
     static constexpr int STAGE = OFF_V + (D / 64) * CHUNK;
     static constexpr int OFF_MISC = NS * STAGE;
-    static constexpr int NBAR = 12;
+    static constexpr int NBAR = 20;
+    static_assert(NS <= 4, "barrier slots hold at most 4 stages");
     static constexpr int OFF_ZP = OFF_MISC + 64 + 8 * NBAR;   // fp32 [8][D] z partials
     static constexpr uint32_t TMEM_COLS = 256;                 // two accumulators of 128 columns
     static constexpr int SMEM = OFF_ZP + 8 * D * 4;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static constexpr int PITCH = D + 1;              // partial-state row pitch (floats)
-    static_assert(128 * PITCH * 4 <= STAGE, "partial state must fit in stage 0");
+    static constexpr int PITCH = D + 4;              // partial-state row pitch (floats; rows 16-byte aligned)
+    static_assert(128 * PITCH * 4 <= NS * STAGE, "partial state must fit in the stage buffers");
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, D, true, true);
     static constexpr int NTHR = 320;
 };
 
-enum { A_FULL = 0, A_PHI = 2, A_EMPTY = 4, A_ACC_FULL = 6, A_ACC_FREE = 8, A_DRAIN = 10 };
+// barrier slots: A_FULL, A_PHI, A_EMPTY have one per stage (NS <= 4)
+enum { A_FULL = 0, A_PHI = 4, A_EMPTY = 8, A_ACC_FULL = 12, A_ACC_FREE = 14, A_DRAIN = 16 };
 
 struct AbsParams {
     int BH, n, CL;
@@ -223,24 +225,29 @@ __global__ void __launch_bounds__(320, 1)
             if (!ok) break;
             uint8_t* st = smem + s * Cfg::STAGE;
             const int tok0 = (t_begin + i) * Cfg::TT;
-            for (int r = rg; r < Cfg::TT; r += NRG) {
+            // all rows are loaded before any is written back (the in-place stores
+            // could otherwise alias the next row's load, serializing the rows);
+            // rows past the last token (a partial tile) become phi = 0
+            constexpr int RPT = Cfg::TT / NRG;   // rows per thread
+            uint32_t kv[RPT];
+#pragma unroll
+            for (int k = 0; k < RPT; ++k)
+                kv[k] = *reinterpret_cast<const uint32_t*>(st + Cfg::OFF_K + coff + sw128_offset(rg + k * NRG, col % 64));
+#pragma unroll
+            for (int k = 0; k < RPT; ++k) {
+                const int r = rg + k * NRG;
+                const bool valid = tok0 + r < p.n;
+                float a = bf16_lo(kv[k]), b = bf16_hi(kv[k]);
+                a = a > 0.0f ? a + 1.0f : __expf(a);
+                b = b > 0.0f ? b + 1.0f : __expf(b);
+                a = valid ? a : 0.0f;
+                b = valid ? b : 0.0f;
+                z0 += a;
+                z1 += b;
+                const uint32_t hi = pack_bf16(a, b);
                 const uint32_t off = coff + sw128_offset(r, col % 64);
-                uint32_t* kp = reinterpret_cast<uint32_t*>(st + Cfg::OFF_K + off);
-                uint32_t* lp = reinterpret_cast<uint32_t*>(st + Cfg::OFF_LO + off);
-                if (tok0 + r < p.n) {
-                    const uint32_t kv = *kp;
-                    float a = bf16_lo(kv), b = bf16_hi(kv);
-                    a = a > 0.0f ? a + 1.0f : __expf(a);
-                    b = b > 0.0f ? b + 1.0f : __expf(b);
-                    z0 += a;
-                    z1 += b;
-                    const uint32_t hi = pack_bf16(a, b);
-                    *kp = hi;
-                    *lp = pack_bf16(a - bf16_lo(hi), b - bf16_hi(hi));
-                } else {
-                    *kp = 0u;
-                    *lp = 0u;
-                }
+                *reinterpret_cast<uint32_t*>(st + Cfg::OFF_K + off) = hi;
+                *reinterpret_cast<uint32_t*>(st + Cfg::OFF_LO + off) = pack_bf16(a - bf16_lo(hi), b - bf16_hi(hi));
             }
             fence_proxy_async_smem();
             mbar_arrive(&bar[A_PHI + s]);
@@ -251,15 +258,28 @@ __global__ void __launch_bounds__(320, 1)
         zp[rg * D + col + 1] = z1;
         // ---- partial state -> shared memory (over stage 0) ----------------
         __syncwarp();
-        float* part = reinterpret_cast<float*>(smem);   // [128][PITCH]
-        // stage 0 may still be read by the producer's last TMA only if this
-        // CTA had a single tile in flight; every load was consumed above.
+        float* part = reinterpret_cast<float*>(smem);   // [128][PITCH], over the stage buffers
+        // every load was consumed above, and the last MMA has been drained.
         if (ok) {
 #pragma unroll
-            for (int k = 0; k < DC; ++k) part[row * Cfg::PITCH + chalf * DC + k] = racc[k];
+            for (int k = 0; k < DC; k += 4)
+                *reinterpret_cast<float4*>(part + row * Cfg::PITCH + chalf * DC + k) =
+                    make_float4(racc[k], racc[k + 1], racc[k + 2], racc[k + 3]);
         } else {
             *wc.abort_flag = 1;
         }
+    }
+    // this rank's rows of S, read while the other CTAs of the cluster finish
+    const int rows_per = (D + p.CL - 1) / p.CL;
+    const int r0 = rank * rows_per, r1 = min(D, r0 + rows_per);
+    float* Sg = p.S + (size_t)bh * D * D;
+    constexpr int ITEMS = (D / 8) * (D / 4) / Cfg::NTHR + 1;   // float4 items per thread (rows_per <= D/8 for CL = 8)
+    float4 s_old[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int e = tid + it * Cfg::NTHR;
+        if (e < (r1 - r0) * (D / 4))
+            s_old[it] = *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / (D / 4)) * D + 4 * (e % (D / 4)));
     }
     tc_fence_before();
     __syncthreads();
@@ -273,18 +293,41 @@ __global__ void __launch_bounds__(320, 1)
     cluster.sync();
     // ---- cluster reduction: rank r owns rows [r0, r1) of S ----------------
     if (*wc.abort_flag == 0) {
-        const int rows_per = (D + p.CL - 1) / p.CL;
-        const int r0 = rank * rows_per, r1 = min(D, r0 + rows_per);
-        float* Sg = p.S + (size_t)bh * D * D;
-        for (int e = tid; e < (r1 - r0) * D; e += Cfg::NTHR) {
-            const int c = r0 + e / D, j = e % D;
-            float acc = 0.0f;
-            for (int q = 0; q < p.CL; ++q) {
-                const float* rp = cluster.map_shared_rank(reinterpret_cast<float*>(smem), q);
-                acc += rp[c * Cfg::PITCH + j];
+        // all ranks' float4s of an item are requested first, then added in rank order;
+        // the first ITEMS items of a thread use the prefetched S, any further ones
+        // (clusters smaller than 8) read S here
+        const int total = (r1 - r0) * (D / 4);
+        auto reduce_item = [&](int e, float4 o) {
+            const int c = r0 + e / (D / 4), j = 4 * (e % (D / 4));
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < p.CL)
+                    v[q] = *reinterpret_cast<const float4*>(
+                        cluster.map_shared_rank(reinterpret_cast<float*>(smem), q) + c * Cfg::PITCH + j);
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q < p.CL) {
+                    acc.x += v[q].x;
+                    acc.y += v[q].y;
+                    acc.z += v[q].z;
+                    acc.w += v[q].w;
+                }
             }
-            Sg[(size_t)c * D + j] += acc;
+            o.x += acc.x;
+            o.y += acc.y;
+            o.z += acc.z;
+            o.w += acc.w;
+            *reinterpret_cast<float4*>(Sg + (size_t)c * D + j) = o;
+        };
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) {
+            const int e = tid + it * Cfg::NTHR;
+            if (e < total) reduce_item(e, s_old[it]);
         }
+        for (int e = tid + ITEMS * Cfg::NTHR; e < total; e += Cfg::NTHR)
+            reduce_item(e, *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / (D / 4)) * D + 4 * (e % (D / 4))));
         if (rank == 0 && tid < D) {
             float acc = 0.0f;
             for (int q = 0; q < p.CL; ++q) acc += cluster.map_shared_rank(zp, q)[7 * D + tid];
@@ -329,14 +372,14 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
 {
     alignas(64) CUtensorMap tk, tv;
     const uint64_t hs = (uint64_t)head_stride * g.d * 2;
-    int e = make_tmap_bf16_3d(&tk, K_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, 128);
+    int e = make_tmap_bf16_3d(&tk, K_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, AbsCfg<128>::TT);
     if (e) return e;
-    e = make_tmap_bf16_3d(&tv, V_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, 128);
+    e = make_tmap_bf16_3d(&tv, V_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, AbsCfg<128>::TT);
     if (e) return e;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int n_tiles = (n_ev + 127) / 128;
+    const int n_tiles = (n_ev + AbsCfg<128>::TT - 1) / AbsCfg<128>::TT;
     int CL = sms / (g.BH > 0 ? g.BH : 1);
     CL = CL < 1 ? 1 : (CL > 8 ? 8 : CL);
     CL = CL > n_tiles ? n_tiles : CL;
