@@ -94,13 +94,22 @@ WsLayout ws_layout(const hf_config* cfg)
     const size_t nqb = (size_t)cfg->chunk_frames * bpf;
     const size_t nkb = (size_t)cfg->window_frames * bpf;
     const size_t kmax = (size_t)cfg->topk < nkb ? (size_t)cfg->topk : nkb;
+    const size_t G = (size_t)(128 / cfg->block_size);             // query blocks per tile
+    const size_t pairs = BH * ((ceil_div((int)nqb, (int)G) + 1) / 2);
     WsLayout w;
+    // the status word and the split counters (both zero between calls) come
+    // first, where a change of topk between calls does not move them
     w.status = 0;
-    w.qp = 1024;
+    w.counters = 1024;
+    w.qp = w.counters + align1k(pairs * 2 * 4);
     w.kp = w.qp + align1k(BH * nqb * d * 4);
     w.idx = w.kp + align1k(BH * nkb * d * 4);
     w.smma = w.idx + align1k(BH * nqb * kmax * 4);
-    w.total = w.smma + align1k(BH * 2 * d * d * 2);
+    w.prounds = w.smma + align1k(BH * 2 * d * d * 2);
+    w.total_compact = w.prounds + align1k(pairs * 4);
+    w.partial = w.total_compact;
+    w.total = w.partial + (size_t)HF_SPLIT_PARTIAL_BYTES(d);
+    static_assert(HF_SPLIT_PARTIAL_BYTES(0) == (size_t)kAttnMaxGrid * 2 * 2 * 128 * 4 * 4, "split buffer sizing");
     return w;
 }
 
@@ -284,7 +293,7 @@ hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_
     float* qp = reinterpret_cast<float*>(w + L.qp);
     float* kp = reinterpret_cast<float*>(w + L.kp);
     HF_LAUNCH(launch_pool(Q, Kc, g, window_frames(sm, n_win), qp, kp, stream), "pool launch");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, stream), "score launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, nullptr, stream), "score launch");
     return HF_OK;
 }
 
@@ -321,8 +330,8 @@ hf_status hf_sparse_swa_attn(const hf_config* cfg, const uint16_t* Q, const uint
     if ((s = check_window(cfg, slot_stride, slot_map, n_win, &sm)) != HF_OK) return s;
     const Geom g = make_geom(cfg, n_win, slot_stride);
     uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + ws_layout(cfg).status);
-    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, nullptr, nullptr, O_swa, nullptr, status, kDefaultWaitLimitNs,
-                          stream),
+    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, nullptr, nullptr, O_swa, nullptr, nullptr, nullptr, nullptr, status,
+                          kDefaultWaitLimitNs, stream),
               "sparse attention launch");
     return HF_OK;
 }
@@ -341,10 +350,16 @@ hf_status hf_linear_read(const hf_config* cfg, const uint16_t* Q, const float* S
     return HF_OK;
 }
 
-hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
-                               int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
-                               const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags,
-                               void* const* events)
+}  // extern "C"
+
+namespace hf {
+
+size_t compact_workspace_bytes(const hf_config* cfg) { return ws_layout(cfg).total_compact; }
+
+hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                       int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S, const float* z,
+                       uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags, void* const* events,
+                       bool allow_split)
 {
     hf_status s = check_cfg(cfg);
     if (s != HF_OK) return s;
@@ -367,6 +382,9 @@ hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const ui
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + L.idx);
     uint16_t* smma = reinterpret_cast<uint16_t*>(w + L.smma);
     uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+    int32_t* prounds = allow_split ? reinterpret_cast<int32_t*>(w + L.prounds) : nullptr;
+    float* partial = allow_split ? reinterpret_cast<float*>(w + L.partial) : nullptr;
+    uint32_t* counters = allow_split ? reinterpret_cast<uint32_t*>(w + L.counters) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // inside a stream capture an event becomes an external record node, so that it
     // also times the graph's replays
@@ -384,14 +402,28 @@ hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const ui
     HF_LAUNCH(mark(0), "event record");
     HF_LAUNCH(launch_pool(Q, Kc, g, pf, qp, kp, stream), "pool launch");
     HF_LAUNCH(mark(1), "event record");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, stream), "score/select launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, prounds, stream), "score/select launch");
     HF_LAUNCH(mark(2), "event record");
     HF_LAUNCH(launch_smma_prep(S, g, smma, stream), "state prep launch");
     HF_LAUNCH(mark(3), "event record");
-    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, smma, z, nullptr, O, status, kDefaultWaitLimitNs, stream),
+    HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, smma, z, nullptr, O, prounds, partial, counters, status,
+                          kDefaultWaitLimitNs, stream),
               "hybrid attention launch");
     HF_LAUNCH(mark(4), "event record");
     return HF_OK;
+}
+
+}  // namespace hf
+
+extern "C" {
+
+hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                               int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
+                               const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags,
+                               void* const* events)
+{
+    return forward_impl(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, flags, events,
+                        true);
 }
 
 hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,

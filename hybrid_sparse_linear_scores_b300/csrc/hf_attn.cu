@@ -88,6 +88,22 @@ __device__ __forceinline__ bool bar_all_or(bool v)
     return r != 0;
 }
 
+// Barrier over one softmax group (128 threads, barrier `id`) that ANDs `v`
+// over the group: every thread gets the same answer.
+__device__ __forceinline__ bool bar_group_and(uint32_t id, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %2, 0;\n\t"
+        "bar.red.and.pred p, %1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 template <uint32_t N>
 __device__ __forceinline__ void reg_alloc()
 {
@@ -150,7 +166,19 @@ enum {
 };
 
 // misc words
-enum { M_TMEM = 0, M_ABORT = 1, M_NLIST = 2, M_LAST = 3 /* 2 */, M_WCOUNT = 8 /* 4 */ };
+enum {
+    M_TMEM = 0,
+    M_ABORT = 1,
+    M_NLIST = 2,
+    M_LAST = 3,      // 2: last list position (+1) that each tile needs
+    M_WCOUNT = 8,    // 4: per-warp counts of the list compaction
+    M_PFIRST = 12,   // split mode: the CTA's first pair, and
+    M_PREF = 13,     //   the global round at which that pair starts
+    M_TOTAL = 14,    //   total rounds of all pairs
+    M_FIRSTR = 16,   // 2: first round of the part that each tile takes part in
+    M_LASTR = 18,    // 2: last such round (-1: none)
+    M_OLD = 20       // 2: arrival count a tile's part found (split pairs)
+};
 
 struct AttnParams {
     Geom g;
@@ -165,7 +193,33 @@ struct AttnParams {
     int pairs_per_head;
     int total_pairs;
     int spf;                // slabs per frame = ceil(nf / 64)
+    // Split mode (all three non-null): every CTA takes an equal share of the
+    // rounds of all pairs; a pair cut between CTAs leaves a partial result per
+    // part, and the part that finishes last merges them.
+    const int32_t* pair_rounds;   // [total_pairs] rounds of each pair's slab stream
+    float* partial;               // [grid][2 slots][2 tiles][d + 4 columns][128 rows]: O, m, l
+    uint32_t* counters;           // [total_pairs][2] parts arrived per tile; zero between launches
 };
+
+// CTA owning global round x when T rounds are cut into G equal shares
+// (CTA c takes rounds [c T / G, (c + 1) T / G)).
+// (32-bit division whenever T * (G + 1) fits, as on every workload of a
+// realistic size; 64-bit otherwise)
+__device__ __forceinline__ int round_owner(uint32_t x, uint32_t T, int G)
+{
+    if ((uint64_t)T * (uint32_t)(G + 1) < (1ull << 32)) return static_cast<int>(((x + 1) * (uint32_t)G - 1) / T);
+    return static_cast<int>((((uint64_t)x + 1) * (uint64_t)G - 1) / T);
+}
+__device__ __forceinline__ uint32_t share_start(int c, uint32_t T, int G)
+{
+    if ((uint64_t)T * (uint32_t)(G + 1) < (1ull << 32)) return (uint32_t)c * T / (uint32_t)G;
+    return static_cast<uint32_t>((uint64_t)c * T / (uint64_t)G);
+}
+// With fewer rounds than CTAs some shares are empty; such a CTA takes no part.
+__device__ __forceinline__ bool share_nonempty(int c, uint32_t T, int G)
+{
+    return share_start(c, T, G) < share_start(c + 1, T, G);
+}
 
 // Round codes: bit (2t + i) of code[r] is set when tile t needs slab i of
 // round r (list position 2r + i).  For one tile, m = (code >> 2t) & 3.
@@ -185,14 +239,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 // number of rounds issued; *ok = false if a wait gave up.
 template <int D, int BETA>
 __device__ __forceinline__ int produce_ring(const CUtensorMap* tm, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                            const uint32_t* list, int n_list, int n_rounds, int bh,
+                                            const uint32_t* list, int n_list, int ra, int rb, int bh,
                                             const AttnParams& p, const WaitCtl& wc, uint32_t site, bool& ok)
 {
     using Cfg = AttnCfg<D, BETA>;
-    int r = 0;
-    for (; r < n_rounds; ++r) {
-        const int s = r % Cfg::NR;
-        if (r >= Cfg::NR && !mbar_wait(&empty[s], ((r / Cfg::NR) - 1) & 1, wc, site)) {
+    int lr = 0;   // rounds are numbered from ra for the stages and phases
+    for (; lr < rb - ra; ++lr) {
+        const int r = ra + lr;
+        const int s = lr % Cfg::NR;
+        if (lr >= Cfg::NR && !mbar_wait(&empty[s], ((lr / Cfg::NR) - 1) & 1, wc, site)) {
             ok = false;
             break;
         }
@@ -208,7 +263,7 @@ __device__ __forceinline__ int produce_ring(const CUtensorMap* tm, uint8_t* ring
                 tma_load_3d(st + m * Cfg::CHUNK + i * (Cfg::SLAB * 128), tm, &full[s], 64 * m, 64 * k, plane);
         }
     }
-    return r;
+    return lr;
 }
 
 template <int D, int BETA, bool FUSED>
@@ -250,6 +305,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = misc[M_TMEM];
 
+    // ---- split mode: the share of all pairs' rounds this CTA takes ----
+    const bool split = p.pair_rounds != nullptr;
+    uint32_t T = 0, s_c = 0, e_c = 0;
+    if (split) {
+        int* tsum = reinterpret_cast<int*>(sK);   // [kThreads]: the key ring is free before the first pair
+        const int NP = p.total_pairs;
+        const int per = (NP + kThreads - 1) / kThreads;
+        const int b0 = min(NP, tid * per), b1 = min(NP, b0 + per);
+        int loc = 0;
+        for (int i = b0; i < b1; ++i) loc += p.pair_rounds[i];
+        tsum[tid] = loc;
+        if (tid == 0) {
+            misc[M_PFIRST] = (uint32_t)NP;   // none, unless found below
+            misc[M_PREF] = 0;
+        }
+        __syncthreads();
+        if (warp == 0) {   // exclusive scan of the kThreads chunk sums
+            constexpr int PL = kThreads / 32;
+            int v[PL], ls = 0;
+#pragma unroll
+            for (int k = 0; k < PL; ++k) {
+                v[k] = tsum[lane * PL + k];
+                ls += v[k];
+            }
+            int inc = ls;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int nb = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                if (lane >= o) inc += nb;
+            }
+            int ex = inc - ls;
+#pragma unroll
+            for (int k = 0; k < PL; ++k) {
+                tsum[lane * PL + k] = ex;
+                ex += v[k];
+            }
+            if (lane == 31) misc[M_TOTAL] = (uint32_t)inc;
+        }
+        __syncthreads();
+        T = misc[M_TOTAL];
+        s_c = share_start(blockIdx.x, T, gridDim.x);
+        e_c = share_start(blockIdx.x + 1, T, gridDim.x);
+        uint32_t P = (uint32_t)tsum[tid];
+        for (int i = b0; i < b1; ++i) {
+            const uint32_t R = (uint32_t)p.pair_rounds[i];
+            if (P <= s_c && s_c < P + R) {
+                misc[M_PFIRST] = (uint32_t)i;
+                misc[M_PREF] = P;
+            }
+            P += R;
+        }
+        __syncthreads();
+    }
+    const int pair_first = split ? (int)misc[M_PFIRST] : (int)blockIdx.x;
+    const uint32_t pref_first = split ? misc[M_PREF] : 0u;
+
     // the tiles of pair `pair`: head bh, first query block qb0[t], blocks nblk[t] (0 = no tile B)
     auto pair_geometry = [&](int pair, int& bh, int (&qb0)[2], int (&nblk)[2]) {
         bh = pair / p.pairs_per_head;
@@ -265,7 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         // ======== warpgroup 0: slab stream, TMA producers, MMA issuer ========
         reg_dealloc<kRegsCtl>();
-        for (int pair = blockIdx.x; pair < p.total_pairs; pair += gridDim.x) {
+        int pair = pair_first;
+        uint32_t P = pref_first;
+        for (;;) {
+            // this part of the pair: rounds [ra, rb) of its stream
+            int ra = 0, rb = 1 << 30;
+            uint32_t R = 0;
+            if (split) {
+                if (pair >= p.total_pairs || P >= e_c || s_c >= e_c) break;
+                R = (uint32_t)p.pair_rounds[pair];
+                ra = (int)(max(s_c, P) - P);
+                rb = (int)(min(e_c, P + R) - P);
+            } else if (pair >= p.total_pairs) {
+                break;
+            }
             int bh, qb0[2], nblk[2];
             pair_geometry(pair, bh, qb0, nblk);
             // ---- barriers (no asynchronous operation is pending here) ----
@@ -347,7 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     base_out += tot;
                     bar_ctl();
                 }
-                if (tid == 0) misc[M_NLIST] = base_out;
+                if (tid == 0) {
+                    misc[M_NLIST] = base_out;
+                    if (split && (uint32_t)(base_out + 1) / 2 != R) report_error(wc, HF_DEV_ERR_CHECK, SITE_ATTN_BAD_INDEX);
+                    misc[M_FIRSTR] = misc[M_FIRSTR + 1] = 0x7FFFFFFFu;
+                    misc[M_LASTR] = misc[M_LASTR + 1] = 0xFFFFFFFFu;
+                }
                 for (int r = tid; r < (base_out + 1) / 2; r += 128) {
                     uint32_t c = 0;
 #pragma unroll
@@ -360,11 +489,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     sCode[r] = static_cast<uint8_t>(c);
                 }
+                bar_ctl();
+                // first and last round of this part that each tile takes part in
+                const int rend = min(rb, (base_out + 1) / 2);
+                for (int r = ra + tid; r < rend; r += 128) {
+                    const uint32_t c = sCode[r];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (tile_bits(c, t)) {
+                            atomicMin(reinterpret_cast<int*>(&misc[M_FIRSTR + t]), r);
+                            atomicMax(reinterpret_cast<int*>(&misc[M_LASTR + t]), r);
+                        }
+                    }
+                }
             }
             // list and barriers ready; a bad index: nothing of this pair is issued
             if (bar_all_or(*wc.abort_flag != 0)) break;
             const int n_list = (int)misc[M_NLIST];
             const int n_rounds = (n_list + 1) / 2;
+            rb = min(rb, n_rounds);
 
             if (warp == 0 && lane == 0) {
                 // ---------- Q tiles, key ring, state operand ----------
@@ -384,12 +527,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int issued = produce_ring<D, BETA>(&tmK, sK, &bar[B_K_FULL], &bar[B_K_EMPTY], sList, n_list,
-                                                         n_rounds, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
+                                                         ra, rb, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
                 bool lin_issued = false;
                 if (FUSED && ok) {
                     // the state operands go into the key ring once every key stage is free
-                    for (int r = max(0, n_rounds - Cfg::NR); r < n_rounds && ok; ++r)
-                        ok = mbar_wait(&bar[B_K_EMPTY + r % Cfg::NR], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_EMPTY);
+                    for (int lr = max(0, rb - ra - Cfg::NR); lr < rb - ra && ok; ++lr)
+                        ok = mbar_wait(&bar[B_K_EMPTY + lr % Cfg::NR], (lr / Cfg::NR) & 1, wc, SITE_ATTN_KV_EMPTY);
                     if (ok) {
                         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.smma) + (size_t)bh * Cfg::LIN_BYTES;
                         mbar_arrive_expect_tx(&bar[B_LIN_FULL], Cfg::LIN_BYTES);
@@ -409,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---------- value ring ----------
                 bool ok = true;
                 const int issued = produce_ring<D, BETA>(&tmV, sV, &bar[B_V_FULL], &bar[B_V_EMPTY], sList, n_list,
-                                                         n_rounds, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
+                                                         ra, rb, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
                 for (int r = max(0, issued - Cfg::NR); r < issued; ++r)
                     drain_wait(&bar[B_V_FULL + r % Cfg::NR], (r / Cfg::NR) & 1, p.wait_limit_ns);
                 if (!ok) *wc.abort_flag = 1;
@@ -430,17 +573,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t q_desc1 = smem_desc(smem_u32(smem + Cfg::OFF_Q + Cfg::Q_BYTES), 16, 1024);
                 const uint64_t k_desc = smem_desc(smem_u32(sK), 16, 1024);
                 const uint64_t v_desc = smem_desc(smem_u32(sV), Cfg::CHUNK, 1024);
-                const int last_round0 = ((int)misc[M_LAST + 0] - 1) >> 1;
-                const int last_round1 = ((int)misc[M_LAST + 1] - 1) >> 1;
+                // last round of this part each tile takes part in (-1: none)
+                const int last_round0 = (int)misc[M_LASTR + 0];
+                const int last_round1 = (int)misc[M_LASTR + 1];
                 int cnt0 = 0, cnt1 = 0;
                 bool first0 = true, first1 = true;
-                int k_round = -1, v_round = -1;   // last round whose key / value stage was waited for
+                int k_round = ra - 1, v_round = ra - 1;   // last round whose key / value stage was waited for
                 // m: the tile's slabs of round r (bit i = slab i), from the round code
+                // stages and phases count rounds from ra
                 auto issue_qk = [&](int r, int t, uint32_t m) -> bool {
                     if (m == 0) return true;
-                    const int s = r % Cfg::NR;
+                    const int s = (r - ra) % Cfg::NR;
                     if (r > k_round) {
-                        if (!mbar_wait(&bar[B_K_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        if (!mbar_wait(&bar[B_K_FULL + s], ((r - ra) / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
                         k_round = r;
                     }
                     tc_fence_after();
@@ -463,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bool& first = t ? first1 : first0;
                     if (!mbar_wait(&bar[B_P_FULL + t], cnt & 1, wc, SITE_ATTN_P_FULL)) return false;
                     ++cnt;
-                    const int s = r % Cfg::NR;
+                    const int s = (r - ra) % Cfg::NR;
                     if (r > v_round) {
-                        if (!mbar_wait(&bar[B_V_FULL + s], (r / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        if (!mbar_wait(&bar[B_V_FULL + s], ((r - ra) / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
                         v_round = r;
                     }
                     tc_fence_after();
@@ -487,21 +632,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 // round codes are read one round ahead of their use
-                uint32_t c_cur = sCode[0];
-                uint32_t c_nxt = n_rounds > 1 ? sCode[1] : 0u;
-                if (ok) ok = issue_qk(0, 0, tile_bits(c_cur, 0)) && issue_qk(0, 1, tile_bits(c_cur, 1));
+                uint32_t c_cur = sCode[ra];
+                uint32_t c_nxt = ra + 1 < rb ? sCode[ra + 1] : 0u;
+                if (ok) ok = issue_qk(ra, 0, tile_bits(c_cur, 0)) && issue_qk(ra, 1, tile_bits(c_cur, 1));
                 if (ok) mma_commit(&bar[B_K_EMPTY + 0]);
-                for (int r = 0; ok && r < n_rounds; ++r) {
-                    const uint32_t c_nn = r + 2 < n_rounds ? sCode[r + 2] : 0u;
-                    const bool more = r + 1 < n_rounds;
+                for (int r = ra; ok && r < rb; ++r) {
+                    const uint32_t c_nn = r + 2 < rb ? sCode[r + 2] : 0u;
+                    const bool more = r + 1 < rb;
                     ok = issue_pv(r, 0, tile_bits(c_cur, 0));
                     if (ok && more) ok = issue_qk(r + 1, 0, tile_bits(c_nxt, 0));
                     if (ok) ok = issue_pv(r, 1, tile_bits(c_cur, 1));
                     if (!ok) break;
-                    mma_commit(&bar[B_V_EMPTY + r % Cfg::NR]);
+                    mma_commit(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
                     if (more) {
                         ok = issue_qk(r + 1, 1, tile_bits(c_nxt, 1));
-                        if (ok) mma_commit(&bar[B_K_EMPTY + (r + 1) % Cfg::NR]);
+                        if (ok) mma_commit(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
                     }
                     c_cur = c_nxt;
                     c_nxt = c_nn;
@@ -545,12 +690,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stop = bar_all_or(*wc.abort_flag != 0);
             tc_fence_after();
             if (stop) break;
+            if (split) {
+                P += R;
+                ++pair;
+            } else {
+                pair += gridDim.x;
+            }
         }
     } else {
         // ======== warpgroups 1 and 2: softmax and epilogue of tile A / tile B ========
         reg_alloc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;
-        for (int pair = blockIdx.x; pair < p.total_pairs; pair += gridDim.x) {
+        int pair = pair_first;
+        uint32_t P = pref_first;
+        for (;;) {
+            // this part of the pair: rounds [ra, rb) of its stream (as in warpgroup 0)
+            int ra = 0, rb = 1 << 30;
+            uint32_t R = 0;
+            if (split) {
+                if (pair >= p.total_pairs || P >= e_c || s_c >= e_c) break;
+                R = (uint32_t)p.pair_rounds[pair];
+                ra = (int)(max(s_c, P) - P);
+                rb = (int)(min(e_c, P + R) - P);
+            } else if (pair >= p.total_pairs) {
+                break;
+            }
             int bh, qb0_[2], nblk_[2];
             pair_geometry(pair, bh, qb0_, nblk_);
             const int qb0 = t ? qb0_[1] : qb0_[0];     // this group's tile
@@ -558,6 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (bar_all_or(*wc.abort_flag != 0)) break;   // list and barriers ready
             const int n_list = (int)misc[M_NLIST];
             const int n_rounds = (n_list + 1) / 2;
+            rb = min(rb, n_rounds);
+            const bool participated = (int)misc[M_LASTR + t] >= 0;   // in a round of this part
             if (nblk > 0) {
                 const int quarter = warp & 3;            // TMEM lane quarter this warp may access
                 const int r = quarter * 32 + lane;       // query row within the tile
@@ -575,14 +741,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t m_nx = 0, e_nx[2] = {0u, 0u};
                 auto find_round = [&](int from) -> int {
                     int rr = from;
-                    while (rr < n_rounds && (m_nx = tile_bits(sCode[rr], t)) == 0u) ++rr;
-                    if (rr < n_rounds) {
+                    while (rr < rb && (m_nx = tile_bits(sCode[rr], t)) == 0u) ++rr;
+                    if (rr < rb) {
                         e_nx[0] = sList[2 * rr + (m_nx == 2u ? 1 : 0)];
                         e_nx[1] = m_nx == 3u ? sList[2 * rr + 1] : 0u;
                     }
                     return rr;
                 };
-                for (int rd = find_round(0); rd < n_rounds; rd = find_round(rd + 1)) {
+                for (int rd = find_round(ra); rd < rb; rd = find_round(rd + 1)) {
                     const int n = m_nx == 3u ? 2 : 1;
                     const uint32_t ent[2] = {e_nx[0], e_nx[1]};
                     // valid columns of this warp's rows in each slab: [0, lo) and [32, 32 + hi)
@@ -715,14 +881,136 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(&bar[B_P_FULL + t]);
                 }
-                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_O_DONE + t], 0, wc, SITE_ATTN_PV_DONE));
-                const float inv_l = 1.0f / ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+                if (ok && participated)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_O_DONE + t], 0, wc, SITE_ATTN_PV_DONE));
+                float l_tot = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+                // ---- a pair cut between CTAs: every part leaves (O, m, l) of each row in
+                // its slot; the part that arrives last merges all parts in part order
+                // (so the result does not depend on which part that is) and finishes
+                // the pair ----
+                bool do_out = true;
+                // the same decision in all four warps: the protocol below has group barriers
+                const bool gok = (FUSED && split) ? bar_group_and(2 + t, ok) : ok;
+                if (FUSED && split && gok) {
+                    const int G = gridDim.x;
+                    // parts: the CTAs c0..c1 with a non-empty share (c0 and c1 own rounds,
+                    // so their shares are never empty)
+                    const int c0 = round_owner(P, T, G);
+                    const int c1 = round_owner(P + R - 1, T, G);
+                    int nparts = 0;
+                    for (int c = c0; c <= c1; ++c) nparts += share_nonempty(c, T, G) ? 1 : 0;
+                    if (nparts > 1) {
+                        // CTA c's block, column-major (a warp's access to one column is one
+                        // 128-byte line): c0 may also end an earlier pair, so it writes
+                        // slot 1 when its share starts before this pair
+                        auto part_col = [&](int c) -> float* {
+                            const int slot = (c == c0 && share_start(c0, T, G) != P) ? 1 : 0;
+                            return p.partial + (((size_t)c * 2 + slot) * 2 + t) * (size_t)((D + 4) * 128) + r;
+                        };
+                        const int me = (int)blockIdx.x;
+                        float* mine = part_col(me);
+                        const float m_own = participated ? m_use : -INFINITY;
+                        const float l_own = participated ? l_tot : 0.0f;
+                        if (participated) tc_fence_after();
+#pragma unroll
+                        for (int cb = 0; cb < D; cb += 64) {
+                            uint32_t o[2][32];
+                            if (participated) {
+                                tmem_ld32_nw(o_col + cb, o[0]);
+                                tmem_ld32_nw(o_col + cb + 32, o[1]);
+                                tmem_wait_ld();
+                                reg_dep32(o[0]);
+                                reg_dep32(o[1]);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) o[0][c] = o[1][c] = 0u;
+                            }
+#pragma unroll
+                            for (int c = 0; c < 64; ++c) __stcg(mine + (cb + c) * 128, __uint_as_float(o[c >> 5][c & 31]));
+                        }
+                        __stcg(mine + D * 128, m_own);
+                        __stcg(mine + (D + 1) * 128, l_own);
+                        asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
+                        if (r == 0) {
+                            __threadfence();
+                            misc[M_OLD + t] = atomicAdd(p.counters + (size_t)pair * 2 + t, 1u);
+                        }
+                        asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
+                        do_out = *reinterpret_cast<volatile uint32_t*>(&misc[M_OLD + t]) == (uint32_t)(nparts - 1);
+                        if (do_out) {
+                            // merge in part order; this CTA's own part comes from TMEM
+                            __threadfence();
+                            float m_all = m_own;
+                            for (int c = c0; c <= c1; ++c)
+                                if (c != me && share_nonempty(c, T, G)) m_all = fmaxf(m_all, __ldcg(part_col(c) + D * 128));
+                            auto scale_of = [&](float mk) { return mk == -INFINITY ? 0.0f : ex2_approx((mk - m_all) * sl2); };
+                            const float sc_own = scale_of(m_own);
+                            float lt = 0.0f;
+#pragma unroll
+                            for (int cb = 0; cb < D; cb += 64) {
+                                float acc[64];
+#pragma unroll
+                                for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+                                for (int c = c0; c <= c1; ++c) {
+                                    if (!share_nonempty(c, T, G)) continue;
+                                    float sc, lk;
+                                    float v[64];
+                                    if (c == me) {
+                                        uint32_t o[2][32];
+                                        if (participated) {
+                                            tmem_ld32_nw(o_col + cb, o[0]);
+                                            tmem_ld32_nw(o_col + cb + 32, o[1]);
+                                            tmem_wait_ld();
+                                            reg_dep32(o[0]);
+                                            reg_dep32(o[1]);
+                                        } else {
+#pragma unroll
+                                            for (int k = 0; k < 32; ++k) o[0][k] = o[1][k] = 0u;
+                                        }
+#pragma unroll
+                                        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(o[k >> 5][k & 31]);
+                                        sc = sc_own;
+                                        lk = l_own;
+                                    } else {
+                                        const float* src = part_col(c);
+#pragma unroll
+                                        for (int k = 0; k < 64; ++k) v[k] = __ldcg(src + (cb + k) * 128);
+                                        const float mk = __ldcg(src + D * 128);
+                                        lk = __ldcg(src + (D + 1) * 128);
+                                        sc = scale_of(mk);
+                                    }
+                                    if (cb == 0) lt = fmaf(sc, lk, lt);
+#pragma unroll
+                                    for (int k = 0; k < 64; ++k) acc[k] = fmaf(sc, v[k], acc[k]);
+                                }
+                                uint32_t o[32];
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc[32 * h + k]);
+                                    tmem_st32(o_col + cb + 32 * h, o);
+                                }
+                            }
+                            l_tot = lt;
+                            tc_fence_before();
+                            if (r == 0) p.counters[(size_t)pair * 2 + t] = 0u;   // ready for the next launch
+                        }
+                    }
+                }
+                const float inv_l = 1.0f / l_tot;
                 if (FUSED) {
                     uint8_t* sQ = smem + Cfg::OFF_Q + t * Cfg::Q_BYTES;
-                    if (ok) {
+                    if (ok && !do_out) {
+                        // another part finishes this pair; the MMA thread still waits for phi(Q)
+                        mbar_arrive(&bar[B_PHIQ + t]);
+                    } else if (ok) {
                         tc_fence_after();
-                        // phi(q) (bf16, in place over Q) and the linear-read denominator
-                        const float* zh = p.z + (size_t)bh * D;
+                        // phi(q) (bf16, in place over Q) and the linear-read denominator; z of
+                        // the head is loaded before the loop (its stores would order the loads)
+                        const float4* zh = reinterpret_cast<const float4*>(p.z + (size_t)bh * D);
+                        float4 zv[D / 4];
+#pragma unroll
+                        for (int i = 0; i < D / 4; ++i) zv[i] = __ldg(zh + i);
                         float den = g.eps;
 #pragma unroll
                         for (int m = 0; m < Cfg::DCH; ++m) {
@@ -739,8 +1027,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     a = a > 0.0f ? a + 1.0f : __expf(a);
                                     bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
                                     w4[i] = pack_bf16(a, bq);
-                                    den = fmaf(bf16_lo(w4[i]), __ldg(zh + c), den);
-                                    den = fmaf(bf16_hi(w4[i]), __ldg(zh + c + 1), den);
+                                    const float4 zq = zv[c >> 2];
+                                    den = fmaf(bf16_lo(w4[i]), (c & 2) ? zq.z : zq.x, den);
+                                    den = fmaf(bf16_hi(w4[i]), (c & 2) ? zq.w : zq.y, den);
                                 }
                                 *ptr = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
@@ -753,28 +1042,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                             const float inv_den = 1.0f / den;
 #pragma unroll
-                            for (int c0 = 0; c0 < D; c0 += 32) {
-                                uint32_t o[32], li[32];
-                                tmem_ld32_nw(o_col + c0, o);
-                                tmem_ld32_nw(s_col + c0, li);
+                            for (int cb = 0; cb < D; cb += 64) {
+                                uint32_t o[2][32], li[2][32];
+                                tmem_ld32_nw(o_col + cb, o[0]);
+                                tmem_ld32_nw(o_col + cb + 32, o[1]);
+                                tmem_ld32_nw(s_col + cb, li[0]);
+                                tmem_ld32_nw(s_col + cb + 32, li[1]);
                                 tmem_wait_ld();
-                                reg_dep32(o);
-                                reg_dep32(li);
-                                uint8_t* rowp = sQ + (c0 >> 6) * (Cfg::TILE_M * 128) + r * 128;
+                                reg_dep32(o[0]);
+                                reg_dep32(o[1]);
+                                reg_dep32(li[0]);
+                                reg_dep32(li[1]);
+                                uint8_t* rowp = sQ + (cb >> 6) * (Cfg::TILE_M * 128) + r * 128;
 #pragma unroll
-                                for (int ch = 0; ch < 4; ++ch) {
+                                for (int ch = 0; ch < 8; ++ch) {   // logical 16-byte chunks of the row
                                     uint32_t w4[4];
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) {
-                                        const int c = ch * 8 + 2 * i;
+                                        const int c = (ch & 3) * 8 + 2 * i;
+                                        const uint32_t* oh = o[ch >> 2];
+                                        const uint32_t* lh = li[ch >> 2];
                                         const float a =
-                                            fmaf(__uint_as_float(o[c]), inv_l, __uint_as_float(li[c]) * inv_den);
-                                        const float bq = fmaf(__uint_as_float(o[c + 1]), inv_l,
-                                                              __uint_as_float(li[c + 1]) * inv_den);
+                                            fmaf(__uint_as_float(oh[c]), inv_l, __uint_as_float(lh[c]) * inv_den);
+                                        const float bq = fmaf(__uint_as_float(oh[c + 1]), inv_l,
+                                                              __uint_as_float(lh[c + 1]) * inv_den);
                                         w4[i] = pack_bf16(a, bq);
                                     }
-                                    const int lch = ((c0 & 63) >> 3) + ch;   // logical 16-byte chunk of the row
-                                    *reinterpret_cast<uint4*>(rowp + (((lch ^ (r & 7)) & 7) << 4)) =
+                                    *reinterpret_cast<uint4*>(rowp + (((ch ^ (r & 7)) & 7) << 4)) =
                                         make_uint4(w4[0], w4[1], w4[2], w4[3]);
                                 }
                             }
@@ -784,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) *wc.abort_flag = 1;
                     // every thread of this softmax group reaches this barrier exactly once
                     asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
-                    if (r == 0 && *wc.abort_flag == 0) {
+                    if (r == 0 && *wc.abort_flag == 0 && do_out) {
                         for (int gb = 0; gb < nblk; ++gb) {
                             const int qbs = qb0 + gb;
                             const int cf = qbs / g.bpf;
@@ -794,7 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              bh * g.C + cf);
                         }
                         bulk_commit();
-                        bulk_wait_all();
+                        bulk_wait_read_all();   // sQ is free again; the writes complete by the end
                     }
                 } else if (ok) {
                     tc_fence_after();
@@ -828,8 +1122,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool stop = bar_all_or(*wc.abort_flag != 0);
             tc_fence_after();
             if (stop) break;
+            if (split) {
+                P += R;
+                ++pair;
+            } else {
+                pair += gridDim.x;
+            }
         }
     }
+    if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait_all();   // the output stores of this CTA
     tc_fence_before();
     bar_all();
     if (warp == 1) {
@@ -854,7 +1155,8 @@ int launch_attn_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMa
 
 int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
                 const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,
-                uint32_t* status, uint64_t wait_limit_ns, void* stream)
+                const int32_t* pair_rounds, float* partial, uint32_t* counters, uint32_t* status,
+                uint64_t wait_limit_ns, void* stream)
 {
     const bool fused = o_bf16 != nullptr;
     const int qrows = g.beta;   // Q / O box rows = one query block
@@ -894,7 +1196,14 @@ int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = p.total_pairs < sms ? p.total_pairs : sms;
+    // split mode (fused forward with the score kernel's pair round counts): one
+    // CTA per SM, each an equal share of all pairs' rounds; otherwise whole pairs
+    // in turn
+    const bool split = fused && pair_rounds && partial && counters;
+    p.pair_rounds = split ? pair_rounds : nullptr;
+    p.partial = split ? partial : nullptr;
+    p.counters = split ? counters : nullptr;
+    const int grid = split ? (sms < kAttnMaxGrid ? sms : kAttnMaxGrid) : (p.total_pairs < sms ? p.total_pairs : sms);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define HF_ATTN_CASE(DD, BB)                                                                       \
     if (g.d == DD && g.beta == BB)                                                                 \

@@ -69,22 +69,31 @@ struct Geom {
 // Workspace layout (byte offsets, 1024-aligned).
 struct WsLayout {
     size_t status;   // 256 B: uint32 [0] code, [1] site
+    size_t counters; // uint32 [BH * pairs per head][2]: parts of a split pair that arrived (zero between calls)
     size_t qp;       // fp32 [BH][nQB][d]
     size_t kp;       // fp32 [BH][W slots][d][bpf]: pooled keys of every ring slot (kept between calls)
     size_t idx;      // int32 [BH][nQB][K_max]
     size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout)
+    size_t prounds;  // int32 [BH * pairs per head]: rounds of each tile pair's slab stream
+    size_t total_compact;   // end of the above: the attention runs without splitting pairs
+    size_t partial;  // fp32 [kAttnMaxGrid][2][2][128][d + 4]: partial results of split pairs
     size_t total;
 };
+
+// Largest attention grid (one CTA per SM, at most this many): the partial
+// results of split pairs are sized for it.
+constexpr int kAttnMaxGrid = 160;
 
 // ---- launchers (return cudaError_t as int) --------------------------------
 int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* qp, float* kpc,
                 void* stream);
 int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                        int32_t* idx, void* stream);
+                        int32_t* idx, int32_t* pair_rounds, void* stream);
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
 int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
                 const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,
-                uint32_t* status, uint64_t wait_limit_ns, void* stream);
+                const int32_t* pair_rounds, float* partial, uint32_t* counters, uint32_t* status,
+                uint64_t wait_limit_ns, void* stream);
 int launch_smma_prep(const float* S, const Geom& g, uint16_t* smma, void* stream);
 int launch_linear_read(const uint16_t* Q, const float* S, const float* z, const Geom& g, float* O, int accumulate,
                        void* stream);
@@ -92,6 +101,15 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
                   float* S, float* z, uint32_t* status, uint64_t wait_limit_ns, void* stream);
 int launch_state_reset(float* S, float* z, const Geom& g, void* stream);
 int launch_selftest_wait(uint32_t* status, uint64_t limit_ns, void* stream);
+
+// The hybrid forward behind hf_hybrid_forward_ex.  allow_split = false runs
+// the attention without cutting tile pairs between CTAs, for a workspace of
+// compact_workspace_bytes() (no partial-result buffer).
+hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
+                       int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S, const float* z,
+                       uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags, void* const* events,
+                       bool allow_split);
+size_t compact_workspace_bytes(const hf_config* cfg);
 
 // Records a printf-style message as the calling thread's hf_last_error()
 // text and returns `code`.

@@ -59,6 +59,7 @@ hf_status hf_hybrid_forward_noalloc(const hf_config* cfg, const uint16_t* Q, con
     size_t need = 0;
     hf_status s = hf_workspace_size(cfg, &need);   // validates cfg
     if (s != HF_OK) return s;
+    need = hf::compact_workspace_bytes(cfg);       // without the buffer for splitting tile pairs
     if (need > (size_t)HF_NOALLOC_SCRATCH_BYTES) {
         return hf::set_last_error(HF_ERR_UNSUPPORTED,
                                   "hf_hybrid_forward_noalloc: this configuration needs %zu bytes of workspace, "
@@ -76,7 +77,8 @@ hf_status hf_hybrid_forward_noalloc(const hf_config* cfg, const uint16_t* Q, con
                                   dev, cudaGetErrorString(e));
     }
     if (status_word) *status_word = ws;
-    return hf_hybrid_forward(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream);
+    return hf::forward_impl(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u, nullptr,
+                            false);
 }
 
 }  // extern "C"

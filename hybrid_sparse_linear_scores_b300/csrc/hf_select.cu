@@ -192,7 +192,7 @@ struct ScoreSmem {
 template <int D, bool WRITE_SCORES, bool SELECT>
 __global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qp, const float* __restrict__ kpc,
                                                            Geom g, SlotMap sm, float* __restrict__ scores,
-                                                           int32_t* __restrict__ idx)
+                                                           int32_t* __restrict__ idx, int32_t* __restrict__ pair_rounds)
 {
     extern __shared__ __align__(16) float smf[];
     float* qps = smf;
@@ -254,6 +254,49 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
         if (warp < nq)
             warp_topk(ss + warp * HF_MAX_KEY_BLOCKS, g.nkb, g.k_eff, idx + ((size_t)bh * g.nqb + qb0 + warp) * g.k_eff);
     }
+    if (SELECT && pair_rounds) {
+        // Rounds of the attention kernel's slab stream for the pairs of tiles this
+        // CTA's query blocks form (a pair = 2 tiles of 128 rows = 256/beta query
+        // blocks, so QG = 8 blocks hold whole pairs): ceil(#slabs in the union of
+        // the pair's selections / 2), with slab k of a frame = rows [64k, 64k+64).
+        const int qpp = 256 / g.beta;               // query blocks per pair
+        const int npairs = (QG + qpp - 1) / qpp;
+        const int spf = (g.nf + 63) / 64;
+        const int nsl = g.n_win * spf;
+        const int words = (nsl + 31) / 32;
+        uint32_t* bits = reinterpret_cast<uint32_t*>(ks);   // [npairs][words], over the staging area
+        __syncthreads();                                     // selections written; staging area free
+        for (int i = tid; i < npairs * words; i += 256) bits[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < nq * g.k_eff; i += 256) {
+            const int q = i / g.k_eff;
+            const int kb = idx[((size_t)bh * g.nqb + qb0 + q) * g.k_eff + (i - q * g.k_eff)];
+            const int w = kb / g.bpf, j = kb - w * g.bpf;
+            uint32_t* pb = bits + (q / qpp) * words;
+            int s0, s1 = -1;
+            if (g.beta == 64) {
+                s0 = w * spf + j;
+            } else if (g.beta == 128) {
+                s0 = w * spf + 2 * j;
+                if (2 * j + 1 < spf) s1 = s0 + 1;
+            } else {
+                s0 = w * spf + (j >> 1);
+            }
+            atomicOr(&pb[s0 >> 5], 1u << (s0 & 31));
+            if (s1 >= 0) atomicOr(&pb[s1 >> 5], 1u << (s1 & 31));
+        }
+        __syncthreads();
+        const int tiles = (g.nqb + 128 / g.beta - 1) / (128 / g.beta);
+        const int pairs_per_head = (tiles + 1) / 2;
+        const int warp = tid / 32, lane = tid & 31;
+        const int pair0 = qb0 / qpp;
+        if (warp < npairs && pair0 + warp < pairs_per_head && warp * qpp < nq) {
+            int cnt = 0;
+            for (int i = lane; i < words; i += 32) cnt += __popc(bits[warp * words + i]);
+            cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+            if (lane == 0) pair_rounds[(size_t)bh * pairs_per_head + pair0 + warp] = (cnt + 1) / 2;
+        }
+    }
 }
 
 // Selection only, from scores in global memory: one warp per row.
@@ -303,29 +346,29 @@ int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const Pool
 
 template <int D, bool W, bool S>
 static int launch_score_t(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                          int32_t* idx, cudaStream_t st)
+                          int32_t* idx, int32_t* pair_rounds, cudaStream_t st)
 {
     auto k = score_select_kernel<D, W, S>;
     cudaError_t e = set_smem(k, ScoreSmem<D>::bytes);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + QG - 1) / QG;
-    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kpc, g, sm, scores, idx);
+    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kpc, g, sm, scores, idx, pair_rounds);
     return (int)cudaGetLastError();
 }
 
 int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                        int32_t* idx, void* stream)
+                        int32_t* idx, int32_t* pair_rounds, void* stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool w = scores != nullptr, s = idx != nullptr;
     if (g.d == 128) {
-        if (w && s) return launch_score_t<128, true, true>(qp, kpc, g, sm, scores, idx, st);
-        if (w) return launch_score_t<128, true, false>(qp, kpc, g, sm, scores, idx, st);
-        return launch_score_t<128, false, true>(qp, kpc, g, sm, scores, idx, st);
+        if (w && s) return launch_score_t<128, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
+        if (w) return launch_score_t<128, true, false>(qp, kpc, g, sm, scores, idx, nullptr, st);
+        return launch_score_t<128, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
     }
-    if (w && s) return launch_score_t<64, true, true>(qp, kpc, g, sm, scores, idx, st);
-    if (w) return launch_score_t<64, true, false>(qp, kpc, g, sm, scores, idx, st);
-    return launch_score_t<64, false, true>(qp, kpc, g, sm, scores, idx, st);
+    if (w && s) return launch_score_t<64, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
+    if (w) return launch_score_t<64, true, false>(qp, kpc, g, sm, scores, idx, nullptr, st);
+    return launch_score_t<64, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
 }
 
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream)

@@ -103,10 +103,14 @@ HF_API const char *hf_last_error(void);
 /* Workspace bytes the forward/scoring/attention/absorb calls need for
  * `cfg` (sized for a full window of cfg->window_frames frames).  The same
  * workspace may be reused by every call on one stream; calls that run
- * concurrently need separate workspaces.  It must be zeroed once before
- * first use (its first 256 bytes are the device status word).  It also holds
- * the pooled-key cache of the layer's ring (see hf_pool_keys): one workspace
- * per ring. */
+ * concurrently need separate workspaces.  Calls that share one may differ
+ * in topk (up to cfg->topk of the sizing call) and in the window, not in the
+ * other fields.  It must be zeroed once before first use (its first 256
+ * bytes are the device status word; counters of the attention kernel's split
+ * pairs follow, which every completed call leaves at zero; after a call that
+ * reported an error, zero the workspace again).  It also holds the
+ * pooled-key cache of the layer's ring (see hf_pool_keys): one workspace per
+ * ring. */
 HF_API hf_status hf_workspace_size(const hf_config *cfg, size_t *bytes /* host */);
 
 /* S = 0, z = 0 (the empty state). */
@@ -225,10 +229,19 @@ HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t
                                             void *const *events /* host, 5 entries */);
 
 /* Size of the static device scratch that hf_hybrid_forward_noalloc uses in
- * place of a workspace: 16 MiB, enough for hf_workspace_size() of a 40-head,
+ * place of a workspace: 16 MiB, enough for the workspace (without its
+ * split-pair part, see below) of a 40-head,
  * d = 128 layer with 1560-token frames, a 9-frame window, 3-frame chunks and
  * block 64 (about 9.5 MB). */
 #define HF_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The last HF_SPLIT_PARTIAL_BYTES(head_dim) bytes of hf_workspace_size() hold
+ * the partial results of tile pairs that the attention kernel cuts between
+ * CTAs to balance its work (every CTA takes an equal share of all pairs'
+ * rounds).  A forward without them runs whole pairs per CTA instead: same
+ * results up to rounding, less even work.  hf_hybrid_forward_noalloc runs
+ * that way. */
+#define HF_SPLIT_PARTIAL_BYTES(head_dim) (160u * 2u * 2u * 128u * ((unsigned)(head_dim) + 4u) * 4u)
 
 /* hf_hybrid_forward for callers that cannot allocate device memory.  The
  * paper has no counterpart: this is a deployment convenience.
@@ -245,9 +258,11 @@ HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t
  *
  *   - Memory: every device that loads the library holds one copy of the
  *     array until the process exits.
- *   - Limit: a configuration whose hf_workspace_size() exceeds
- *     HF_NOALLOC_SCRATCH_BYTES is rejected with HF_ERR_UNSUPPORTED before
- *     anything is launched; use hf_hybrid_forward for it.
+ *   - Limit: the scratch stands in for the workspace without its split-pair
+ *     part (hf_workspace_size() - HF_SPLIT_PARTIAL_BYTES(head_dim)); a
+ *     configuration that needs more than HF_NOALLOC_SCRATCH_BYTES is rejected
+ *     with HF_ERR_UNSUPPORTED before anything is launched; use
+ *     hf_hybrid_forward for it.
  *   - Set-up: the first call on a device (the calling thread's current
  *     device, which must be the device of `stream` and of the buffers) looks
  *     up the array's device address with cudaGetSymbolAddress, which may load
