@@ -30,7 +30,9 @@
 //   warp 2     TMA producer of the values (a second ring of NR round stages).
 //              Keys are released as soon as Q K^T has read them, values
 //              after P V: each ring runs about NR rounds ahead.
-//   warp 1     TMEM owner + single-thread MMA issuer, in the order
+//   warp 1     TMEM owner + MMA issuer (the whole warp runs converged, one
+//              elected lane issues: the operands stay warp-uniform and the
+//              issue keeps pace with the tensor core), in the order
 //                QK_A(0) QK_B(0) | PV_A(r) QK_A(r+1) PV_B(r) QK_B(r+1) | ...
 //              so that the tensor core works on one tile while the other
 //              tile's softmax runs:
@@ -556,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = max(0, issued - Cfg::NR); r < issued; ++r)
                     drain_wait(&bar[B_V_FULL + r % Cfg::NR], (r / Cfg::NR) & 1, p.wait_limit_ns);
                 if (!ok) *wc.abort_flag = 1;
-            } else if (warp == 1 && lane == 0) {
-                // ---------- MMA issuer ----------
+            } else if (warp == 1) {
+                // ---------- MMA issuer (the whole warp, converged; one elected lane issues) ----------
                 // Batches in the order A(-1) B(-1) A(0) B(0) A(1) ..., batch t(r) =
                 // P V_t(r) followed by Q K^T_t(r+1) (S_t is free again once P V_t(r) has
                 // been issued: the tensor core executes in issue order).  Each tile's
@@ -565,7 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // batch.  The MMA queue holds only a few MMAs, so the thread keeps the
                 // work between batches short: round codes are read ahead, and each
                 // round's key and value stages are waited for once.
-                bool ok = mbar_wait(&bar[B_Q], 0, wc, SITE_ATTN_Q);
+                // waits are polled by every lane and agreed on, so the warp stays converged
+                auto wait_all = [&](uint64_t* b, uint32_t parity, uint32_t site) -> bool {
+                    return __all_sync(0xFFFFFFFFu, mbar_wait(b, parity, wc, site));
+                };
+                bool ok = wait_all(&bar[B_Q], 0, SITE_ATTN_Q);
                 tc_fence_after();
                 // base descriptors (start addresses advance in 16-byte units): Q tiles and
                 // the key ring K-major, the value ring MN-major (64-column chunks CHUNK apart)
@@ -585,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (m == 0) return true;
                     const int s = (r - ra) % Cfg::NR;
                     if (r > k_round) {
-                        if (!mbar_wait(&bar[B_K_FULL + s], ((r - ra) / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        if (!wait_all(&bar[B_K_FULL + s], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL)) return false;
                         k_round = r;
                     }
                     tc_fence_after();
@@ -597,20 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dt = tmem + 256 * t + 128;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(dt, qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
+                        mma_ss_warp(dt, qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
                                kd + (uint64_t)(((kk >> 2) * Cfg::CHUNK + (kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
-                    mma_commit(&bar[B_S_FULL + t]);
+                    mma_commit_warp(&bar[B_S_FULL + t]);
                     return true;
                 };
                 auto issue_pv = [&](int r, int t, uint32_t m) -> bool {
                     if (m == 0) return true;
                     int& cnt = t ? cnt1 : cnt0;
                     bool& first = t ? first1 : first0;
-                    if (!mbar_wait(&bar[B_P_FULL + t], cnt & 1, wc, SITE_ATTN_P_FULL)) return false;
+                    if (!wait_all(&bar[B_P_FULL + t], cnt & 1, SITE_ATTN_P_FULL)) return false;
                     ++cnt;
                     const int s = (r - ra) % Cfg::NR;
                     if (r > v_round) {
-                        if (!mbar_wait(&bar[B_V_FULL + s], ((r - ra) / Cfg::NR) & 1, wc, SITE_ATTN_KV_FULL)) return false;
+                        if (!wait_all(&bar[B_V_FULL + s], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL)) return false;
                         v_round = r;
                     }
                     tc_fence_after();
@@ -624,18 +630,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t at = o_tm + 128 + 32 * j;
 #pragma unroll
                         for (int kk = 0; kk < Cfg::SLAB / 16; ++kk)
-                            mma_ts(o_tm, at + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), Cfg::IDESC_PV,
+                            mma_ts_warp(o_tm, at + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), Cfg::IDESC_PV,
                                    (first && j == 0 && kk == 0) ? 0u : 1u);
                     }
                     first = false;
-                    if (r == (t ? last_round1 : last_round0)) mma_commit(&bar[B_O_DONE + t]);
+                    if (r == (t ? last_round1 : last_round0)) mma_commit_warp(&bar[B_O_DONE + t]);
                     return true;
                 };
                 // round codes are read one round ahead of their use
                 uint32_t c_cur = sCode[ra];
                 uint32_t c_nxt = ra + 1 < rb ? sCode[ra + 1] : 0u;
                 if (ok) ok = issue_qk(ra, 0, tile_bits(c_cur, 0)) && issue_qk(ra, 1, tile_bits(c_cur, 1));
-                if (ok) mma_commit(&bar[B_K_EMPTY + 0]);
+                if (ok) mma_commit_warp(&bar[B_K_EMPTY + 0]);
                 for (int r = ra; ok && r < rb; ++r) {
                     const uint32_t c_nn = r + 2 < rb ? sCode[r + 2] : 0u;
                     const bool more = r + 1 < rb;
@@ -643,20 +649,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok && more) ok = issue_qk(r + 1, 0, tile_bits(c_nxt, 0));
                     if (ok) ok = issue_pv(r, 1, tile_bits(c_cur, 1));
                     if (!ok) break;
-                    mma_commit(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
+                    mma_commit_warp(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
                     if (more) {
                         ok = issue_qk(r + 1, 1, tile_bits(c_nxt, 1));
-                        if (ok) mma_commit(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
+                        if (ok) mma_commit_warp(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
                     }
                     c_cur = c_nxt;
                     c_nxt = c_nn;
                 }
                 if (FUSED && ok) {
-                    ok = mbar_wait(&bar[B_LIN_FULL], 0, wc, SITE_ATTN_LIN);
+                    ok = wait_all(&bar[B_LIN_FULL], 0, SITE_ATTN_LIN);
                     const uint64_t l_desc = smem_desc(smem_u32(sK), D * 128, 1024);
                     for (int t = 0; ok && t < 2; ++t) {
                         if (nblk[t] == 0) continue;
-                        ok = mbar_wait(&bar[B_PHIQ + t], 0, wc, SITE_ATTN_PHIQ);
+                        ok = wait_all(&bar[B_PHIQ + t], 0, SITE_ATTN_PHIQ);
                         if (!ok) break;
                         tc_fence_after();
                         const uint64_t qd = t ? q_desc1 : q_desc0;
@@ -664,16 +670,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int hl = 0; hl < 2; ++hl) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(tmem + 256 * t + 128,
+                                mma_ss_warp(tmem + 256 * t + 128,
                                        qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
                                        l_desc + (uint64_t)((hl * (D * D * 2) + kk * 2048) >> 4), Cfg::IDESC_LIN,
                                        (hl > 0 || kk > 0) ? 1u : 0u);
                         }
-                        mma_commit(&bar[B_LIN_DONE + t]);
+                        mma_commit_warp(&bar[B_LIN_DONE + t]);
                     }
                 }
                 // drain: every MMA this thread issued has completed before the pair ends
-                mma_commit(&bar[B_DRAIN]);
+                mma_commit_warp(&bar[B_DRAIN]);
                 const uint32_t a = smem_u32(&bar[B_DRAIN]);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(a, 0)) {
