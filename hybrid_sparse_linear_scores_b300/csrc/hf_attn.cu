@@ -13,7 +13,7 @@
 // block for beta = 128, two blocks for beta = 32).
 //
 // The grid is persistent: one CTA per SM, each CTA takes PAIRS of adjacent
-// tiles of one head (A and B) in turn.  The two tiles share one stream of
+// tiles of one head (A and B).  The two tiles share one stream of
 // slabs -- the union of both tiles' slabs in window order -- so a slab that
 // both need is loaded once.  The stream is cut into rounds of two slabs; a
 // tile takes part in a round when it needs one or both of its slabs.  The
@@ -21,6 +21,15 @@
 // tile needs both, Q K^T is one N = 128 MMA per K step (an N = 64 MMA reads
 // as many operand bytes from shared memory per FLOP as it computes, and runs
 // at about half the tensor core's rate).
+//
+// Balancing (fused forward).  Pairs differ in length (their union of
+// selections), so whole pairs per CTA leave a long tail.  Instead every CTA
+// takes an equal share of all pairs' rounds (the score kernel counts each
+// pair's rounds): CTA c runs rounds [cT/G, (c+1)T/G) of the T rounds of the
+// G CTAs, cutting at most two pairs.  Each part of a cut pair leaves its
+// (O, m, l) rows in a column-major workspace block; the part that arrives
+// last (a per-pair counter) merges all parts in part order -- the result does
+// not depend on the order of arrival -- and runs the epilogue.
 //
 // Warp roles (384 threads = 3 warpgroups, 1 CTA per SM):
 //   warps 0-3  build the pair's slab stream; then
