@@ -25,8 +25,9 @@
 // Balancing (fused forward).  Pairs differ in length (their union of
 // selections), so whole pairs per CTA leave a long tail.  Instead every CTA
 // takes an equal share of all pairs' rounds (the score kernel counts each
-// pair's rounds): CTA c runs rounds [cT/G, (c+1)T/G) of the T rounds of the
-// G CTAs, cutting at most two pairs.  Each part of a cut pair leaves its
+// pair's rounds), each pair counted with a few extra units for the fixed cost
+// of a part: CTA c runs the rounds in units [cT/G, (c+1)T/G) of the T units
+// of the G CTAs, cutting at most two pairs.  Each part of a cut pair leaves its
 // (O, m, l) rows in a column-major workspace block; the part that arrives
 // last (a per-pair counter) merges all parts in part order -- the result does
 // not depend on the order of arrival -- and runs the epilogue.
@@ -212,6 +213,12 @@ struct AttnParams {
     uint32_t* counters;           // [total_pairs][2] parts arrived per tile; zero between launches
 };
 
+// Balancing units: each pair counts kPartUnits units ahead of its rounds, so
+// that the fixed cost of a part (list build, pipeline fill, epilogue: about
+// eight rounds' time on the realistic workload) is shared out too; round x of
+// a pair whose units start at P is unit P + kPartUnits + x.
+constexpr uint32_t kPartUnits = 8;
+
 // CTA owning global round x when T rounds are cut into G equal shares
 // (CTA c takes rounds [c T / G, (c + 1) T / G)).
 // (32-bit division whenever T * (G + 1) fits, as on every workload of a
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int per = (NP + kThreads - 1) / kThreads;
         const int b0 = min(NP, tid * per), b1 = min(NP, b0 + per);
         int loc = 0;
-        for (int i = b0; i < b1; ++i) loc += p.pair_rounds[i];
+        for (int i = b0; i < b1; ++i) loc += p.pair_rounds[i] + (int)kPartUnits;
         tsum[tid] = loc;
         if (tid == 0) {
             misc[M_PFIRST] = (uint32_t)NP;   // none, unless found below
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         e_c = share_start(blockIdx.x + 1, T, gridDim.x);
         uint32_t P = (uint32_t)tsum[tid];
         for (int i = b0; i < b1; ++i) {
-            const uint32_t R = (uint32_t)p.pair_rounds[i];
+            const uint32_t R = (uint32_t)p.pair_rounds[i] + kPartUnits;   // units of the pair
             if (P <= s_c && s_c < P + R) {
                 misc[M_PFIRST] = (uint32_t)i;
                 misc[M_PREF] = P;
@@ -394,10 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ra = 0, rb = 1 << 30;
             uint32_t R = 0;
             if (split) {
-                if (pair >= p.total_pairs || P >= e_c || s_c >= e_c) break;
+                if (pair >= p.total_pairs || P + kPartUnits >= e_c || s_c >= e_c) break;
                 R = (uint32_t)p.pair_rounds[pair];
-                ra = (int)(max(s_c, P) - P);
-                rb = (int)(min(e_c, P + R) - P);
+                const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
+                ra = (int)(max(s_c, Pr) - Pr);
+                rb = (int)(min(e_c, Pr + R) - Pr);
             } else if (pair >= p.total_pairs) {
                 break;
             }
@@ -706,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (stop) break;
             if (split) {
-                P += R;
+                P += R + kPartUnits;
                 ++pair;
             } else {
                 pair += gridDim.x;
@@ -723,10 +731,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int ra = 0, rb = 1 << 30;
             uint32_t R = 0;
             if (split) {
-                if (pair >= p.total_pairs || P >= e_c || s_c >= e_c) break;
+                if (pair >= p.total_pairs || P + kPartUnits >= e_c || s_c >= e_c) break;
                 R = (uint32_t)p.pair_rounds[pair];
-                ra = (int)(max(s_c, P) - P);
-                rb = (int)(min(e_c, P + R) - P);
+                const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
+                ra = (int)(max(s_c, Pr) - Pr);
+                rb = (int)(min(e_c, Pr + R) - Pr);
             } else if (pair >= p.total_pairs) {
                 break;
             }
@@ -910,8 +919,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int G = gridDim.x;
                     // parts: the CTAs c0..c1 with a non-empty share (c0 and c1 own rounds,
                     // so their shares are never empty)
-                    const int c0 = round_owner(P, T, G);
-                    const int c1 = round_owner(P + R - 1, T, G);
+                    const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
+                    const int c0 = round_owner(Pr, T, G);
+                    const int c1 = round_owner(Pr + R - 1, T, G);
                     int nparts = 0;
                     for (int c = c0; c <= c1; ++c) nparts += share_nonempty(c, T, G) ? 1 : 0;
                     if (nparts > 1) {
@@ -919,7 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // 128-byte line): c0 may also end an earlier pair, so it writes
                         // slot 1 when its share starts before this pair
                         auto part_col = [&](int c) -> float* {
-                            const int slot = (c == c0 && share_start(c0, T, G) != P) ? 1 : 0;
+                            const int slot = (c == c0 && share_start(c0, T, G) != Pr) ? 1 : 0;
                             return p.partial + (((size_t)c * 2 + slot) * 2 + t) * (size_t)((D + 4) * 128) + r;
                         };
                         const int me = (int)blockIdx.x;
@@ -1138,7 +1148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (stop) break;
             if (split) {
-                P += R;
+                P += R + kPartUnits;
                 ++pair;
             } else {
                 pair += gridDim.x;
