@@ -439,15 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nsl = g.n_win * p.spf;
             for (int i = tid; i < (nsl + 1) / 2; i += 128) sMask[i] = 0;
             bar_ctl();
-            for (int t = 0; t < 2; ++t) {
-                const int total = nblk[t] * g.k_eff;
-                const int32_t* ip = p.idx + ((size_t)bh * g.nqb + qb0[t]) * g.k_eff;
-                for (int i = tid; i < total; i += 128) {
+            {
+                // entry i of tile t: query block i / k_eff of the tile, key block kb
+                auto mark = [&](int t, int i, int kb) {
                     const int gq = i / g.k_eff;
-                    const int kb = ip[i];
                     if (kb < 0 || kb >= g.nkb) {
                         report_error(wc, HF_DEV_ERR_CHECK, SITE_ATTN_BAD_INDEX);
-                        continue;
+                        return;
                     }
                     const int w = kb / g.bpf;
                     const int j = kb - w * g.bpf;
@@ -463,7 +461,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int s = w * p.spf + (j >> 1);
                         atomicOr(&sMask[s >> 1], (1u << (8 * t + 4 * (j & 1) + gq)) << ((s & 1) * 16));
                     }
+                };
+                int total[2];
+                const int32_t* ip[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    total[t] = nblk[t] * g.k_eff;
+                    ip[t] = p.idx + ((size_t)bh * g.nqb + qb0[t]) * g.k_eff;
                 }
+                // the first 128 entries of both tiles in one memory round trip
+                const int kb0 = tid < total[0] ? __ldg(ip[0] + tid) : 0;
+                const int kb1 = tid < total[1] ? __ldg(ip[1] + tid) : 0;
+                if (tid < total[0]) mark(0, tid, kb0);
+                if (tid < total[1]) mark(1, tid, kb1);
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+                    for (int i = tid + 128; i < total[t]; i += 128) mark(t, i, __ldg(ip[t] + i));
             }
             bar_ctl();
             {   // ordered compaction of the slabs that either tile needs
@@ -1030,35 +1043,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(&bar[B_PHIQ + t]);
                     } else if (ok) {
                         tc_fence_after();
-                        // phi(q) (bf16, in place over Q) and the linear-read denominator; z of
-                        // the head is loaded before the loop (its stores would order the loads)
+                        // phi(q) (bf16, in place over Q) and the linear-read denominator.  The
+                        // row is loaded whole, transformed in registers (z read alongside, four
+                        // independent denominator chains) and stored whole: a store between
+                        // the loads would order every later load behind it.
                         const float4* zh = reinterpret_cast<const float4*>(p.z + (size_t)bh * D);
-                        float4 zv[D / 4];
+                        uint4 qv[Cfg::DCH * 8];   // 16-byte chunk k = channels [8k, 8k + 8)
 #pragma unroll
-                        for (int i = 0; i < D / 4; ++i) zv[i] = __ldg(zh + i);
-                        float den = g.eps;
+                        for (int k = 0; k < Cfg::DCH * 8; ++k)
+                            qv[k] = *reinterpret_cast<const uint4*>(sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 +
+                                                                    ((((k & 7) ^ (r & 7)) & 7) << 4));
+                        float dn[4] = {g.eps, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                        for (int m = 0; m < Cfg::DCH; ++m) {
-                            uint8_t* rowp = sQ + m * (Cfg::TILE_M * 128) + r * 128;
+                        for (int k = 0; k < Cfg::DCH * 8; ++k) {
+                            const float4 za = __ldg(zh + 2 * k), zb = __ldg(zh + 2 * k + 1);
+                            const float zc[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+                            uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
 #pragma unroll
-                            for (int ch = 0; ch < 8; ++ch) {
-                                uint4* ptr = reinterpret_cast<uint4*>(rowp + (((ch ^ (r & 7)) & 7) << 4));
-                                uint4 v = *ptr;
-                                uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const int c = m * 64 + ch * 8 + 2 * i;
-                                    float a = bf16_lo(w4[i]), bq = bf16_hi(w4[i]);
-                                    a = a > 0.0f ? a + 1.0f : __expf(a);
-                                    bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
-                                    w4[i] = pack_bf16(a, bq);
-                                    const float4 zq = zv[c >> 2];
-                                    den = fmaf(bf16_lo(w4[i]), (c & 2) ? zq.z : zq.x, den);
-                                    den = fmaf(bf16_hi(w4[i]), (c & 2) ? zq.w : zq.y, den);
-                                }
-                                *ptr = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            for (int i = 0; i < 4; ++i) {
+                                float a = bf16_lo(w4[i]), bq = bf16_hi(w4[i]);
+                                a = a > 0.0f ? a + 1.0f : __expf(a);
+                                bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
+                                w4[i] = pack_bf16(a, bq);
+                                dn[i] = fmaf(bf16_lo(w4[i]), zc[2 * i], dn[i]);
+                                dn[i] = fmaf(bf16_hi(w4[i]), zc[2 * i + 1], dn[i]);
                             }
+                            qv[k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                         }
+                        const float den = (dn[0] + dn[1]) + (dn[2] + dn[3]);
+#pragma unroll
+                        for (int k = 0; k < Cfg::DCH * 8; ++k)
+                            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 +
+                                                      ((((k & 7) ^ (r & 7)) & 7) << 4)) = qv[k];
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(&bar[B_PHIQ + t]);
