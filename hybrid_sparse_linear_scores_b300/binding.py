@@ -67,6 +67,7 @@ def lib():
             "hf_hybrid_forward_ex": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_uint32,
                                       ctypes.POINTER(ctypes.c_void_p)], _I),
             "hf_pool_keys": ([cfgp, _P, _I, _P, _I, _P, _P], _I),
+            "hf_ring_write": ([cfgp, _P, _P, _P, _P, _I, _P, _I, _P], _I),
             "hf_get_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
             "hf_selftest_wait_timeout": ([_P, _I, _P], _I),
         }
@@ -197,6 +198,17 @@ def hf_pool_keys(cfg, Kc, slot_stride, slots, ws, stream=None):
     sl = _slots(list(slots))
     _check(lib().hf_pool_keys(ctypes.byref(cfg), _ptr(Kc), int(slot_stride), sl and sl[0], len(list(slots)),
                               _ptr(ws), _stream(stream)), "hf_pool_keys")
+
+
+def hf_ring_write(cfg, K_src, V_src, Kc, Vc, slot_stride, slots, stream=None):
+    """Copy a chunk's K, V ([BH, n, N_f, d], device or pinned host) into ring slots."""
+    slots = list(slots)
+    for t in (K_src, V_src):
+        if hasattr(t, "is_contiguous") and not t.is_contiguous():
+            raise ValueError("hf_ring_write: sources must be contiguous")
+    sl = _slots(slots)
+    _check(lib().hf_ring_write(ctypes.byref(cfg), _ptr(K_src), _ptr(V_src), _ptr(Kc), _ptr(Vc), int(slot_stride),
+                               sl[0], len(slots), _stream(stream)), "hf_ring_write")
 
 
 def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, flags=0, events=None,

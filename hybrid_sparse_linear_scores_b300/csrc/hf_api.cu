@@ -443,6 +443,44 @@ hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint1
                                 nullptr);
 }
 
+hf_status hf_ring_write(const hf_config* cfg, const uint16_t* K_src, const uint16_t* V_src, uint16_t* Kc, uint16_t* Vc,
+                        int32_t slot_stride, const int32_t* slots, int32_t n_frames, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(K_src);
+    HF_CHECK_PTR(V_src);
+    HF_CHECK_PTR(Kc);
+    HF_CHECK_PTR(Vc);
+    if (n_frames < 1 || n_frames > cfg->window_frames)
+        return fail(HF_ERR_INVALID_ARG, "n_frames %d not in [1, window_frames %d]", n_frames, cfg->window_frames);
+    if (slot_stride < cfg->tokens_per_frame)
+        return fail(HF_ERR_INVALID_ARG, "slot_stride %d < tokens_per_frame %d", slot_stride, cfg->tokens_per_frame);
+    if (!slots) return fail(HF_ERR_INVALID_ARG, "slots is NULL");
+    uint64_t used = 0;
+    for (int i = 0; i < n_frames; ++i) {
+        const int sl = slots[i];
+        if (sl < 0 || sl >= cfg->window_frames)
+            return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d outside [0, %d)", i, sl, cfg->window_frames);
+        if (used & (1ull << sl)) return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d given twice", i, sl);
+        used |= 1ull << sl;
+    }
+    const size_t BH = (size_t)cfg->batch * cfg->heads;
+    const size_t d = (size_t)cfg->head_dim;
+    const size_t frame = (size_t)cfg->tokens_per_frame * d;                 // elements of one frame of one head
+    const size_t spitch = (size_t)n_frames * frame * 2;                     // bytes between heads in the source
+    const size_t dpitch = (size_t)cfg->window_frames * slot_stride * d * 2; // bytes between heads in the ring
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int f = 0; f < n_frames; ++f) {
+        const size_t doff = (size_t)slots[f] * slot_stride * d;
+        HF_LAUNCH(cudaMemcpy2DAsync(Kc + doff, dpitch, K_src + f * frame, spitch, frame * 2, BH, cudaMemcpyDefault, st),
+                  "ring write (K)");
+        HF_LAUNCH(cudaMemcpy2DAsync(Vc + doff, dpitch, V_src + f * frame, spitch, frame * 2, BH, cudaMemcpyDefault, st),
+                  "ring write (V)");
+    }
+    return HF_OK;
+}
+
 hf_status hf_pool_keys(const hf_config* cfg, const uint16_t* Kc, int32_t slot_stride, const int32_t* slots,
                        int32_t n_slots, void* ws, void* stream)
 {

@@ -91,12 +91,10 @@ class HybridAttentionLayer:
         return [(self.frames + c) % self.R for c in range(self.C)]
 
     def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor, stream=None):
-        """K_new, V_new: [BH, C, N_f, d] bf16 for the next C frames.  The
-        chunk's key blocks are pooled into the cache right after the copy."""
+        """K_new, V_new: contiguous [BH, C, N_f, d] bf16 for the next C frames.
+        The chunk's key blocks are pooled into the cache right after the copy."""
         slots = self.chunk_slots()
-        for c, slot in enumerate(slots):
-            self.Kc[:, slot, :self.nf].copy_(K_new[:, c])
-            self.Vc[:, slot, :self.nf].copy_(V_new[:, c])
+        hb.hf_ring_write(self.cfg, K_new, V_new, self.Kc, self.Vc, self.ss, slots, stream)
         self.pool_slots(slots, stream)
         self.frames += self.C
 
@@ -193,9 +191,8 @@ class HostStreamer:
             self.h2d.wait_event(self.ev_absorb)
             self.h2d.wait_event(self.ev_fwd[b])
             self.Qd[b].copy_(Qh, non_blocking=True)
-            for c, slot in enumerate(slots):
-                L.Kc[:, slot, :L.nf].copy_(Kh[:, c], non_blocking=True)
-                L.Vc[:, slot, :L.nf].copy_(Vh[:, c], non_blocking=True)
+            # one pitched copy per frame and tensor straight from the pinned buffers
+            hb.hf_ring_write(L.cfg, Kh, Vh, L.Kc, L.Vc, L.ss, slots, self.h2d)
             self.ev_h2d[b].record(self.h2d)
         self.h2d_bytes += (Qh.numel() + Kh.numel() + Vh.numel()) * 2
         # 2. compute: absorb the frames this chunk's arrival evicts (they are

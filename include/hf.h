@@ -197,6 +197,22 @@ HF_API hf_status hf_hybrid_forward(const hf_config *cfg, const uint16_t *Q, cons
 HF_API hf_status hf_pool_keys(const hf_config *cfg, const uint16_t *Kc, int32_t slot_stride,
                               const int32_t *slots /* host */, int32_t n_slots, void *ws, void *stream);
 
+/* Writes a chunk's keys and values into the K/V ring (the sliding window of
+ * English technical summary, section 2.A.2: a new chunk's frames take the
+ * slots of the frames it evicts, which must already have been absorbed).
+ * K_src, V_src: bf16 [b, H, n_frames, tokens_per_frame, d], contiguous, in
+ * device memory or in host memory (pinned host memory lets the copy run
+ * asynchronously and overlap other work); Kc, Vc: the ring, bf16
+ * [b, H, W, slot_stride, d] in device memory (W = cfg->window_frames slots).
+ * Frame f goes to rows [0, tokens_per_frame) of slot slots[f] (host array of
+ * n_frames distinct slots in [0, W), 1 <= n_frames <= W).  One pitched copy
+ * per frame and tensor (rows = heads), asynchronous on `stream`; the caller
+ * keeps the sources alive until the stream reaches this point.  Pooled keys
+ * of the written slots are stale afterwards: call hf_pool_keys for them. */
+HF_API hf_status hf_ring_write(const hf_config *cfg, const uint16_t *K_src, const uint16_t *V_src,
+                               uint16_t *Kc, uint16_t *Vc, int32_t slot_stride,
+                               const int32_t *slots /* host */, int32_t n_frames, void *stream);
+
 /* Flags of hf_hybrid_forward_ex. */
 #define HF_FWD_CACHED_KEYS 1u  /* take the window's pooled keys from the cache
                                   (every slot of the window pooled by hf_pool_keys,

@@ -101,6 +101,21 @@ def test_absorb_and_topk_argument_errors():
     hb.hf_absorb_evicted(cfg, FAKE, FAKE, None, None, 0, FAKE, stream=0)
 
 
+@pytest.mark.parametrize("kw,msg", [
+    (dict(K_src=0), "K_src is NULL"), (dict(Vc=0), "Vc is NULL"), (dict(slots=[]), "n_frames"),
+    (dict(slots=[0, 0]), "given twice"), (dict(slots=[9]), "outside"), (dict(slots=[-1]), "outside"),
+    (dict(slot_stride=100), "slot_stride"),
+])
+def test_ring_write_argument_errors_are_synchronous(kw, msg):
+    cfg = cfg_of(CONFIGS["realistic"])
+    a = dict(K_src=FAKE, V_src=FAKE, Kc=FAKE, Vc=FAKE, slot_stride=cfg.tokens_per_frame, slots=[0, 1, 2])
+    a.update(kw)
+    with pytest.raises(hb.HFError) as ei:
+        hb.hf_ring_write(cfg, a["K_src"], a["V_src"], a["Kc"], a["Vc"], a["slot_stride"], a["slots"], stream=0)
+    assert ei.value.code == 1
+    assert msg in str(ei.value)
+
+
 def test_header_documents_every_entry_point():
     """Every declared function carries a comment block in the header."""
     text = open(hb.HEADER).read()

@@ -129,3 +129,28 @@ def test_host_streamer_matches_layer_steps(cuda_device):
     for s in range(w.steps):
         assert torch.equal(outs_host[s].view(torch.int16), outs_ref[s].cpu().view(torch.int16)), f"chunk {s}"
     assert torch.equal(L.S, ref.S) and torch.equal(L.z, ref.z)
+
+
+@pytest.mark.parametrize("where", ["pinned_host", "device"])
+def test_ring_write_places_frames(where, cuda_device):
+    """hf_ring_write puts frame f of every head into rows [0, N_f) of ring
+    slot slots[f], bit for bit, from pinned host memory or from device
+    memory, and leaves the other slots and the padding rows of the written
+    slots (slot_stride > N_f) untouched."""
+    from hybrid_sparse_linear_scores_b300 import binding as hb
+    BH, nf, d, R, ss, C = 6, 100, 64, 7, 112, 3
+    cfg = hb.make_config(1, BH, d, nf, R, C, 64, 4)
+    gen = torch.Generator().manual_seed(5)
+    K = torch.randn(BH, C, nf, d, generator=gen).to(torch.bfloat16)
+    V = torch.randn(BH, C, nf, d, generator=gen).to(torch.bfloat16)
+    Ks, Vs = (K.pin_memory(), V.pin_memory()) if where == "pinned_host" else (K.to(cuda_device), V.to(cuda_device))
+    slots = [5, 0, 3]
+    fill = torch.full((BH, R, ss, d), 7.0, dtype=torch.bfloat16)
+    Kc, Vc = fill.to(cuda_device), fill.to(cuda_device)
+    hb.hf_ring_write(cfg, Ks, Vs, Kc, Vc, ss, slots, torch.cuda.current_stream(cuda_device))
+    torch.cuda.synchronize()
+    for src, ring in ((K, Kc), (V, Vc)):
+        ref = fill.clone()
+        for f, sl in enumerate(slots):
+            ref[:, sl, :nf] = src[:, f]
+        assert torch.equal(ring.cpu().view(torch.int16), ref.view(torch.int16))
