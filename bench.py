@@ -50,6 +50,7 @@ sys.path.insert(0, ROOT)
 METRIC = "hybrid-attn layer µs per latent frame & effective TFLOP/s (% bf16 TC peak), 1 B300"
 WORKLOAD = "realistic"
 L2_FLUSH_BYTES = 256 << 20
+DENOISE_STEPS = 4          # "few-step" denoising per chunk (the pages give no number)
 
 
 # --------------------------------------------------------------------------
@@ -336,6 +337,78 @@ def build_layer(w, cfg, dev, spare_slots: int = 0):
     return L, Kw, Vw
 
 
+def time_graph(fn, dev, flush, n):
+    """Mean ms of `fn(stream)` captured as one CUDA graph, L2 flushed before each replay."""
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.stream(cap):
+        fn(cap)                                                   # untimed first launch on this stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fn(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        flush.zero_()
+        g.replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
+def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush, step_ms, args):
+    """Two more figures on the same box, beside the step:
+    - denoise_reuse: a chunk denoised in DENOISE_STEPS steps.  The window's
+      K/V and the state do not change between the steps of one chunk, so
+      absorb and key pooling run once and the forward once per step.
+    - dense_swa_w21: the plain sliding-window attention the method replaces
+      (W = 21 frames, every key block selected, empty state: the method's own
+      dense special case), same chunk, same kernels."""
+    from hybrid_sparse_linear_scores_b300 import binding as hb
+    from hybrid_sparse_linear_scores_b300 import synth
+    from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, frames_tensor
+    n = min(args.steps, 100)
+    out = {}
+
+    def chunk(stream):
+        L.absorb_slots(evict_slot, w.chunk_frames, stream)
+        L.pool_slots(chunk_slots, stream)
+        for _ in range(DENOISE_STEPS):
+            L.forward(Q, O, idx, stream)
+    ms_chunk = time_graph(chunk, dev, flush, n)
+    L.check_device_status()
+    out["denoise_reuse"] = {"denoise_steps": DENOISE_STEPS, "ms_per_chunk": ms_chunk,
+                            "us_per_latent_frame": 1000 * ms_chunk / w.chunk_frames,
+                            "reading": "'few-step' denoising taken as 4 steps per chunk",
+                            "how": "one CUDA graph per chunk: absorb + key pooling once, then 4 forwards"}
+
+    wd = CONFIGS["dense_w21"]
+    cfg_d = hb.make_config(wd.batch, wd.heads, wd.head_dim, wd.tokens_per_frame, wd.window_frames,
+                           wd.chunk_frames, wd.block_size, wd.k_for(0))
+    Ld, _, _ = build_layer(wd, cfg_d, dev)
+    Ld.pool_slots(Ld.slot_map())
+    Qd = frames_tensor(wd, synth.STREAM_Q, wd.chunk(0), dev).reshape(wd.heads_total, -1, wd.head_dim)
+    Od = torch.empty_like(Qd)
+    idx_d = torch.empty((wd.heads_total, wd.n_qb(), wd.k_for(0)), dtype=torch.int32, device=dev)
+    ms_d = time_graph(lambda st: Ld.forward(Qd, Od, idx_d, st), dev, flush, n)
+    Ld.check_device_status()
+    nq, nk = wd.chunk_frames * wd.tokens_per_frame, wd.window_frames * wd.tokens_per_frame
+    fl_d = 4.0 * wd.head_dim * nq * nk * wd.heads_total
+    out["dense_swa_w21"] = {"workload": workload_desc(wd), "ms_per_chunk": ms_d,
+                            "us_per_latent_frame": 1000 * ms_d / wd.chunk_frames,
+                            "attention_tflops": fl_d / (ms_d * 1e-3) / 1e12,
+                            "hybrid_step_speedup": ms_d / step_ms,
+                            "how": "hf_hybrid_forward_ex (cached key pools) with topk = all blocks and S = z = 0, "
+                                   "one CUDA graph, L2 flushed before each replay"}
+    del Ld
+    return out
+
+
 def run_hf(args):
     ws, rank, local = dist_env()
     dev = torch.device("cuda", local)
@@ -478,6 +551,10 @@ def run_hf(args):
                       "copied back, on copy streams overlapped with the neighbouring chunks' compute; "
                       f"host wall clock over {n_e2e} chunks"}
 
+    extra = {}
+    if not args.skip_extras:
+        extra = extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush, ms, args)
+
     pk = peaks()
     attn_ms = statistics.mean(times["attention"])
     attn_tf = (fl["attn"] + fl["lin"]) / (attn_ms * 1e-3) / 1e12
@@ -510,6 +587,7 @@ def run_hf(args):
         "clocks": clocks,
         "wall_s_timed_region": t_wall,
     }
+    line.update(extra)
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and ws == 1 and not args.skip_cpu_baseline:
@@ -530,6 +608,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-extras", action="store_true", help="skip the denoise-reuse and dense-baseline figures")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

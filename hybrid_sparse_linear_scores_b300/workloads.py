@@ -151,6 +151,10 @@ CONFIGS: dict[str, Workload] = {
                        topk_frac=0.25, steps=80),
     "wide": Workload("wide", 1, 40, 128, 1560, 3, 9, 64, seed=4, recipe="frame_mean",
                      topk_frac=0.25, absorbed_frames=60),
+    # the dense sliding-window baseline that the method replaces: W = 21 frames,
+    # every key block selected, nothing in the state
+    "dense_w21": Workload("dense_w21", 1, 12, 128, 1560, 3, 21, 64, seed=5, recipe="frame_mean",
+                          topk_frac=1.0),
 }
 
 

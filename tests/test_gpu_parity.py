@@ -64,18 +64,20 @@ def test_tiny_stream_every_step(cuda_device):
         compare(O, ref["O"], what=f"tiny step {s}")
 
 
-@pytest.mark.parametrize("name", ["realistic", "wide"])
+@pytest.mark.parametrize("name", ["realistic", "wide", "dense_w21"])
 def test_full_config_sampled_rows(name, cuda_device):
-    """Full size: all indices exact; outputs on rows sampled over every tile."""
+    """Full size: all indices exact; outputs on rows sampled over every tile.
+    dense_w21 is the dense sliding-window baseline (W = 21, every block
+    selected, empty state)."""
     w = CONFIGS[name]
     st = Step(w, 0, cuda_device)
     O, idx = st.run_forward()
     rows = sample_rows(w, 160)
     heads = list(range(w.heads_total)) if w.heads_total <= 12 else list(range(0, w.heads_total, 5))
     S, z = st.oracle_state()
-    sub = Step.__new__(Step)
     ref = oracle.hybrid_forward(st.Q[heads].cpu(), flat(st.Kwin[heads]).cpu(), flat(st.Vwin[heads]).cpu(),
-                                S[heads], z[heads], C=w.chunk_frames, n_win=w.n_win(0), nf=w.tokens_per_frame,
+                                None if S is None else S[heads], None if z is None else z[heads],
+                                C=w.chunk_frames, n_win=w.n_win(0), nf=w.tokens_per_frame,
                                 beta=w.block_size, k=w.k_for(0), rows=rows)
     np.testing.assert_array_equal(idx[heads].cpu().numpy(), ref["idx"])
     compare(O[heads][:, rows], ref["O"], what=name)
