@@ -44,6 +44,7 @@ def _load():
                                            _P, _I, _P, _P, _P, _P, _P]
         lib.hfo_hybrid_forward.restype = _I
         lib.hfo_max_threads.restype = _I
+        lib.hfo_rope_relative.argtypes = [_P, _I, _I, _I, _I, _P, _I, _I, _D, _P]
         _lib = lib
     return _lib
 
@@ -173,6 +174,18 @@ def hybrid_forward(Q, K, V, S, z, *, C: int, n_win: int, nf: int, beta: int, k: 
     if margin:
         out["margin"] = mg
     return out
+
+
+def rope_relative(x, offsets, max_offset: int, rot_dims: int, base: float = 10000.0) -> np.ndarray:
+    """Relative temporal RoPE (step 8 of hf_oracle.c).  x: bf16 [BH, F, N_f, d];
+    offsets: frame offsets inside the window (length F).  Returns fp64."""
+    xb = _bf16_bits(x)
+    BH, F, nf, d = xb.shape
+    off = np.ascontiguousarray(offsets, np.int32)
+    assert off.shape == (F,)
+    y = np.empty((BH, F, nf, d), np.float64)
+    _load().hfo_rope_relative(_ptr(xb), BH, F, nf, d, _ptr(off), int(max_offset), int(rot_dims), float(base), _ptr(y))
+    return y
 
 
 def state_from_frames(Kev, Vev, S=None, z=None) -> tuple[np.ndarray, np.ndarray]:

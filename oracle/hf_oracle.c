@@ -44,6 +44,15 @@
  *     final output is the sum of the compressed history and the sparse
  *     local attention).
  *
+ *  8. Relative temporal RoPE (English technical summary, section 2.C
+ *     "Stability Enhancements": temporal RoPE indices are kept under a fixed
+ *     upper bound in training and inference, positions taken as relative
+ *     offsets).  Readings taken: the rotary embedding of Su et al.
+ *     (RoFormer, 2021) on channel pairs (2i, 2i+1), i < rot_dims/2, angle
+ *     p * base^(-2i/rot_dims); the temporal index p of a token is its
+ *     frame's offset inside the current window, clamped to [0, max_offset];
+ *     channels >= rot_dims pass unchanged.  Double precision.
+ *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fno-fast-math -shared -fPIC.
  * -ffp-contract=off keeps every float add and multiply separately rounded;
  * fmaf() is the C library's correctly rounded fused multiply-add.
@@ -355,4 +364,27 @@ int hfo_hybrid_forward(int BH, const uint16_t *Q, const uint16_t *K, const uint1
         free(lbuf); free(pq); free(ol); free(os);
     }
     return 0;
+}
+
+/* Step 8: x [BH][F][nf][d] bf16 -> y fp64, frame f rotated by the clamped
+ * offset offsets[f]. */
+void hfo_rope_relative(const uint16_t *x, int BH, int F, int nf, int d, const int32_t *offsets,
+                       int max_offset, int rot_dims, double base, double *y)
+{
+    for (int h = 0; h < BH; ++h)
+        for (int f = 0; f < F; ++f) {
+            int p = offsets[f];
+            if (p < 0) p = 0;
+            if (p > max_offset) p = max_offset;
+            for (int t = 0; t < nf; ++t) {
+                const size_t row = (((size_t)h * F + f) * nf + t) * d;
+                for (int c = 0; c < d; ++c) y[row + c] = bf16_to_float(x[row + c]);
+                for (int i = 0; i < rot_dims / 2; ++i) {
+                    const double ang = (double)p * pow(base, -2.0 * i / rot_dims);
+                    const double x0 = y[row + 2 * i], x1 = y[row + 2 * i + 1];
+                    y[row + 2 * i] = x0 * cos(ang) - x1 * sin(ang);
+                    y[row + 2 * i + 1] = x0 * sin(ang) + x1 * cos(ang);
+                }
+            }
+        }
 }

@@ -348,3 +348,71 @@ def test_generator_moments_and_frame_independence():
     assert torch.equal(a[:, 2:3], b)
     x = a.double()
     assert abs(float(x.mean())) < 0.02 and abs(float(x.std()) - 1.0) < 0.02
+
+
+# ---- relative temporal RoPE (English technical summary, section 2.C) --------
+
+def test_rope_identity_and_passthrough():
+    """Offset 0 is the identity; channels at and above rot_dims never move.
+    Catches an index shift (rotating frame 0) or rotating every channel."""
+    rng = np.random.default_rng(3)
+    x = bf16(rng.normal(size=(2, 3, 4, 16)))
+    xd = x.double().numpy()
+    y = oracle.rope_relative(x, [0, 2, 5], max_offset=6, rot_dims=8)
+    assert np.array_equal(y[:, 0], xd[:, 0])
+    assert np.array_equal(y[..., 8:], xd[..., 8:])
+
+
+def test_rope_preserves_pair_norms():
+    """Catches a wrong sign or swapped term in the 2x2 rotation."""
+    rng = np.random.default_rng(4)
+    x = bf16(rng.normal(size=(1, 4, 3, 32)))
+    xd = x.double().numpy()
+    y = oracle.rope_relative(x, [0, 1, 3, 9], max_offset=9, rot_dims=32)
+    n_x = xd[..., 0::2] ** 2 + xd[..., 1::2] ** 2
+    n_y = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    np.testing.assert_allclose(n_y, n_x, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_scores_depend_on_relative_offset_only():
+    """q.k after rotation depends only on the offset difference of the two
+    frames (the property that makes window-relative indices valid).  Catches
+    an angle that is not linear in the offset or that differs between q and k."""
+    rng = np.random.default_rng(5)
+    q = bf16(rng.normal(size=(1, 1, 1, 64)))
+    k = bf16(rng.normal(size=(1, 1, 1, 64)))
+    def dot(a, b):
+        qa = oracle.rope_relative(q, [a], 20, 64)[0, 0, 0]
+        kb = oracle.rope_relative(k, [b], 20, 64)[0, 0, 0]
+        return float(qa @ kb)
+    for a, b in [(3, 1), (8, 0), (5, 5)]:
+        for s in (1, 4, 9):
+            assert abs(dot(a + s, b + s) - dot(a, b)) < 1e-9
+    # equal offsets: the rotation is orthogonal, the plain product comes back
+    assert abs(dot(7, 7) - float(q.double().numpy().ravel() @ k.double().numpy().ravel())) < 1e-9
+    # and the offset difference does matter
+    assert abs(dot(6, 0) - dot(0, 0)) > 1e-3
+
+
+def test_rope_frequency_schedule():
+    """At offset 1 a unit vector in pair i turns by base^(-2i/rot_dims):
+    1 rad for pair 0, then a constant ratio base^(-2/rot_dims) per pair.
+    Catches a wrong exponent (e.g. -i/rot_dims) or a pair/channel mix-up."""
+    rot, base = 16, 10000.0
+    x = np.zeros((1, 1, 1, rot), np.float32)
+    x[..., 0::2] = 1.0
+    y = oracle.rope_relative(bf16(x), [1], 4, rot, base)[0, 0, 0]
+    ang = np.arctan2(y[1::2], y[0::2])
+    assert abs(ang[0] - 1.0) < 1e-12
+    np.testing.assert_allclose(ang[1:] / ang[:-1], base ** (-2.0 / rot), rtol=1e-9)
+
+
+def test_rope_offsets_are_clamped():
+    """Offsets above the bound act as the bound; negative ones as 0.  Catches
+    a missing clamp (the upper bound on temporal indices)."""
+    rng = np.random.default_rng(6)
+    x = bf16(rng.normal(size=(1, 1, 2, 8)))
+    a = oracle.rope_relative(x, [25], 6, 8)
+    b = oracle.rope_relative(x, [6], 6, 8)
+    assert np.array_equal(a, b)
+    assert np.array_equal(oracle.rope_relative(x, [-3], 6, 8), x.double().numpy())
