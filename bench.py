@@ -51,6 +51,7 @@ METRIC = "hybrid-attn layer µs per latent frame & effective TFLOP/s (% bf16 TC 
 WORKLOAD = "realistic"
 L2_FLUSH_BYTES = 256 << 20
 DENOISE_STEPS = 4          # "few-step" denoising per chunk (the pages give no number)
+ROPE_BASE = 10000.0        # rotary base frequency of the RoPE pre-step (the pages give none)
 
 
 # --------------------------------------------------------------------------
@@ -362,13 +363,15 @@ def time_graph(fn, dev, flush, n):
 
 
 def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush, step_ms, args):
-    """Two more figures on the same box, beside the step:
+    """More figures on the same box, beside the step:
     - denoise_reuse: a chunk denoised in DENOISE_STEPS steps.  The window's
       K/V and the state do not change between the steps of one chunk, so
       absorb and key pooling run once and the forward once per step.
     - dense_swa_w21: the plain sliding-window attention the method replaces
       (W = 21 frames, every key block selected, empty state: the method's own
-      dense special case), same chunk, same kernels."""
+      dense special case), same chunk, same kernels.
+    - rope_prestep: the relative temporal RoPE pre-step on the chunk's
+      queries and the window's keys (HBM-bound)."""
     from hybrid_sparse_linear_scores_b300 import binding as hb
     from hybrid_sparse_linear_scores_b300 import synth
     from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, frames_tensor
@@ -386,6 +389,30 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
                             "us_per_latent_frame": 1000 * ms_chunk / w.chunk_frames,
                             "reading": "'few-step' denoising taken as 4 steps per chunk",
                             "how": "one CUDA graph per chunk: absorb + key pooling once, then 4 forwards"}
+
+    # relative temporal RoPE pre-step: the chunk's queries (offsets W-C..W-1) in
+    # place, the window's keys from the unrotated ring into a rotated copy
+    Wn = w.n_win(0)
+    Qr = Q.clone()
+    Kr = torch.empty_like(L.Kc)
+    nfd = w.tokens_per_frame * w.head_dim
+    q_off = list(range(Wn - w.chunk_frames, Wn))
+
+    def rope(stream):
+        hb.hf_rope_relative(L.cfg, Qr, Qr, w.chunk_frames * nfd, nfd, list(range(w.chunk_frames)), q_off, Wn - 1,
+                            w.head_dim, ROPE_BASE, stream)
+        hb.hf_rope_relative(L.cfg, L.Kc, Kr, L.R * L.ss * w.head_dim, L.ss * w.head_dim, L.slot_map(),
+                            list(range(Wn)), Wn - 1, w.head_dim, ROPE_BASE, stream)
+    ms_rope = time_graph(rope, dev, flush, n)
+    rope_bytes = 2 * (w.chunk_frames + Wn) * w.heads_total * nfd * 2
+    hbm = peaks()["hbm_gbs"]
+    out["rope_prestep"] = {"ms_per_step": ms_rope, "bytes": rope_bytes,
+                           "GB_s": rope_bytes / (ms_rope * 1e-3) / 1e9,
+                           "hbm_frac": rope_bytes / (ms_rope * 1e-3) / 1e9 / hbm,
+                           "how": "hf_rope_relative on the chunk's Q (in place) and the window's K (ring -> rotated "
+                                  "copy), offsets relative to the window, bound W-1, all channels, base 10000; "
+                                  "2 launches in one CUDA graph, L2 flushed before each replay"}
+    del Qr, Kr
 
     wd = CONFIGS["dense_w21"]
     cfg_d = hb.make_config(wd.batch, wd.heads, wd.head_dim, wd.tokens_per_frame, wd.window_frames,

@@ -68,6 +68,8 @@ def lib():
                                       ctypes.POINTER(ctypes.c_void_p)], _I),
             "hf_pool_keys": ([cfgp, _P, _I, _P, _I, _P, _P], _I),
             "hf_ring_write": ([cfgp, _P, _P, _P, _P, _I, _P, _I, _P], _I),
+            "hf_rope_relative": ([cfgp, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, _P, _I, _I, _I,
+                                  ctypes.c_float, _P], _I),
             "hf_get_device_status": ([_P, _P, ctypes.POINTER(_I)], _I),
             "hf_selftest_wait_timeout": ([_P, _I, _P], _I),
         }
@@ -209,6 +211,19 @@ def hf_ring_write(cfg, K_src, V_src, Kc, Vc, slot_stride, slots, stream=None):
     sl = _slots(slots)
     _check(lib().hf_ring_write(ctypes.byref(cfg), _ptr(K_src), _ptr(V_src), _ptr(Kc), _ptr(Vc), int(slot_stride),
                                sl[0], len(slots), _stream(stream)), "hf_ring_write")
+
+
+def hf_rope_relative(cfg, src, dst, head_stride, frame_stride, slots, offsets, max_offset, rot_dims,
+                     theta_base=10000.0, stream=None):
+    """Relative temporal RoPE of frames slots[f] (offset offsets[f], clamped to
+    [0, max_offset]); strides in elements; dst may be src."""
+    slots, offsets = list(slots), list(offsets)
+    if len(slots) != len(offsets):
+        raise ValueError("hf_rope_relative: one offset per frame")
+    sl, of = _slots(slots), _slots(offsets)
+    _check(lib().hf_rope_relative(ctypes.byref(cfg), _ptr(src), _ptr(dst), int(head_stride), int(frame_stride),
+                                  sl and sl[0], of and of[0], len(slots), int(max_offset), int(rot_dims),
+                                  float(theta_base), _stream(stream)), "hf_rope_relative")
 
 
 def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, flags=0, events=None,

@@ -443,6 +443,56 @@ hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint1
                                 nullptr);
 }
 
+hf_status hf_rope_relative(const hf_config* cfg, const uint16_t* src, uint16_t* dst, int64_t head_stride,
+                           int64_t frame_stride, const int32_t* slots, const int32_t* offsets, int32_t n_frames,
+                           int32_t max_offset, int32_t rot_dims, float theta_base, void* stream)
+{
+    hf_status s = check_cfg(cfg);
+    if (s != HF_OK) return s;
+    HF_CHECK_PTR(src);
+    HF_CHECK_PTR(dst);
+    const int d = cfg->head_dim;
+    if (n_frames < 1 || n_frames > HF_MAX_WINDOW_FRAMES)
+        return fail(HF_ERR_INVALID_ARG, "n_frames %d not in [1, %d]", n_frames, HF_MAX_WINDOW_FRAMES);
+    if (!slots || !offsets) return fail(HF_ERR_INVALID_ARG, "slots / offsets is NULL");
+    if (rot_dims < 0 || rot_dims > d || rot_dims % 8 != 0)
+        return fail(HF_ERR_INVALID_ARG, "rot_dims %d not a multiple of 8 in [0, head_dim %d]", rot_dims, d);
+    if (max_offset < 0) return fail(HF_ERR_INVALID_ARG, "max_offset %d < 0", max_offset);
+    if (!(theta_base > 1.0f) || !(theta_base < 3.0e38f))
+        return fail(HF_ERR_INVALID_ARG, "theta_base must be finite and > 1");
+    if (head_stride % 8 != 0 || frame_stride % 8 != 0)
+        return fail(HF_ERR_INVALID_ARG, "strides must be multiples of 8 elements");
+    if (frame_stride < (int64_t)cfg->tokens_per_frame * d)
+        return fail(HF_ERR_INVALID_ARG, "frame_stride %lld < tokens_per_frame * head_dim",
+                    (long long)frame_stride);
+    RopeParams p;
+    p.src = src;
+    p.dst = dst;
+    p.head_stride = head_stride;
+    p.frame_stride = frame_stride;
+    p.BH = cfg->batch * cfg->heads;
+    p.n_frames = n_frames;
+    p.nf = cfg->tokens_per_frame;
+    p.d = d;
+    p.rot_dims = rot_dims;
+    uint64_t used = 0;
+    int32_t max_slot = 0;
+    for (int f = 0; f < n_frames; ++f) {
+        if (slots[f] < 0 || slots[f] >= 64) return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d outside [0, 64)", f, slots[f]);
+        if (used & (1ull << slots[f])) return fail(HF_ERR_INVALID_ARG, "slots[%d] = %d given twice", f, slots[f]);
+        used |= 1ull << slots[f];
+        max_slot = slots[f] > max_slot ? slots[f] : max_slot;
+        p.slot[f] = slots[f];
+        p.pos[f] = offsets[f] < 0 ? 0 : (offsets[f] > max_offset ? max_offset : offsets[f]);
+    }
+    if (head_stride < (int64_t)(max_slot + 1) * frame_stride)
+        return fail(HF_ERR_INVALID_ARG, "head_stride %lld smaller than the frames it holds", (long long)head_stride);
+    for (int i = 0; i < 64; ++i)
+        p.inv_freq[i] = i < rot_dims / 2 ? (float)pow((double)theta_base, -2.0 * i / rot_dims) : 0.0f;
+    HF_LAUNCH(launch_rope(p, stream), "rope launch");
+    return HF_OK;
+}
+
 hf_status hf_ring_write(const hf_config* cfg, const uint16_t* K_src, const uint16_t* V_src, uint16_t* Kc, uint16_t* Vc,
                         int32_t slot_stride, const int32_t* slots, int32_t n_frames, void* stream)
 {

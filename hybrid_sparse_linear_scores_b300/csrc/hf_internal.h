@@ -95,6 +95,19 @@ int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const
                 const int32_t* pair_rounds, float* partial, uint32_t* counters, uint32_t* status,
                 uint64_t wait_limit_ns, void* stream);
 int launch_smma_prep(const float* S, const Geom& g, uint16_t* smma, void* stream);
+
+// Relative temporal RoPE pre-step: element (h, f, t, c) at
+// h * head_stride + slot[f] * frame_stride + t * d + c (src and dst alike).
+struct RopeParams {
+    const uint16_t* src;
+    uint16_t* dst;
+    int64_t head_stride, frame_stride;      // elements
+    int BH, n_frames, nf, d, rot_dims;
+    int32_t slot[HF_MAX_WINDOW_FRAMES];     // frame f's position along frame_stride
+    int32_t pos[HF_MAX_WINDOW_FRAMES];      // frame f's clamped offset
+    float inv_freq[64];                     // base^(-2i / rot_dims), i < rot_dims / 2
+};
+int launch_rope(const RopeParams& p, void* stream);
 int launch_linear_read(const uint16_t* Q, const float* S, const float* z, const Geom& g, float* O, int accumulate,
                        void* stream);
 int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int64_t head_stride, const Geom& g,

@@ -213,6 +213,27 @@ HF_API hf_status hf_ring_write(const hf_config *cfg, const uint16_t *K_src, cons
                                uint16_t *Kc, uint16_t *Vc, int32_t slot_stride,
                                const int32_t *slots /* host */, int32_t n_frames, void *stream);
 
+/* Relative temporal RoPE pre-step (English technical summary, section 2.C
+ * "Stability Enhancements": temporal RoPE indices are held under one fixed
+ * upper bound in training and inference, positions taken as relative
+ * offsets).  Rotary embedding (RoFormer) on channel pairs (2i, 2i+1),
+ * i < rot_dims/2: angle p * theta_base^(-2i/rot_dims), where p is the
+ * frame's offset inside the current window (offsets[f], host) clamped to
+ * [0, max_offset]; channels >= rot_dims are copied unchanged.  src, dst: bf16
+ * (device), element (h, f, t, c) at h*head_stride + slots[f]*frame_stride +
+ * t*head_dim + c, t < tokens_per_frame (rows between tokens_per_frame and
+ * the frame stride are not touched); dst may equal src (in place).  slots:
+ * host array of n_frames distinct values in [0, 64).  rot_dims: multiple of
+ * 8 in [0, head_dim]; strides: multiples of 8 elements.  Rotate the chunk's
+ * queries and the window's keys (from an unrotated ring into a rotated copy,
+ * so that no stored value is rotated twice) before the forward; the values
+ * and the linear state are not rotated.  Asynchronous on `stream`. */
+HF_API hf_status hf_rope_relative(const hf_config *cfg, const uint16_t *src, uint16_t *dst,
+                                  int64_t head_stride, int64_t frame_stride,
+                                  const int32_t *slots /* host */, const int32_t *offsets /* host */,
+                                  int32_t n_frames, int32_t max_offset, int32_t rot_dims,
+                                  float theta_base, void *stream);
+
 /* Flags of hf_hybrid_forward_ex. */
 #define HF_FWD_CACHED_KEYS 1u  /* take the window's pooled keys from the cache
                                   (every slot of the window pooled by hf_pool_keys,

@@ -122,3 +122,22 @@ def test_header_documents_every_entry_point():
     for name in hb.declared_functions():
         m = re.search(r"/\*(?:(?!\*/).)*\*/\s*HF_API[^;]*\b" + name + r"\s*\(", text, re.S)
         assert m, name
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(src=0), "src is NULL"), (dict(rot_dims=12), "rot_dims"), (dict(rot_dims=136), "rot_dims"),
+    (dict(max_offset=-1), "max_offset"), (dict(theta_base=1.0), "theta_base"), (dict(frame_stride=1560 * 128 + 4), "multiples of 8"),
+    (dict(frame_stride=64), "frame_stride"), (dict(slots=[0, 0], offsets=[0, 1]), "given twice"),
+    (dict(slots=[64], offsets=[0]), "outside"), (dict(head_stride=1560 * 128), "head_stride"),
+    (dict(slots=[], offsets=[]), "n_frames"),
+])
+def test_rope_argument_errors_are_synchronous(kw, msg):
+    cfg = cfg_of(CONFIGS["realistic"])
+    a = dict(src=FAKE, dst=FAKE, head_stride=9 * 1560 * 128, frame_stride=1560 * 128, slots=[0, 1, 2],
+             offsets=[6, 7, 8], max_offset=8, rot_dims=128, theta_base=10000.0)
+    a.update(kw)
+    with pytest.raises(hb.HFError) as ei:
+        hb.hf_rope_relative(cfg, a["src"], a["dst"], a["head_stride"], a["frame_stride"], a["slots"], a["offsets"],
+                            a["max_offset"], a["rot_dims"], a["theta_base"], stream=0)
+    assert ei.value.code == 1
+    assert msg in str(ei.value)
