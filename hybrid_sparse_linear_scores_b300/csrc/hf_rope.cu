@@ -8,7 +8,8 @@
 // current window clamped to [0, max_offset]; channels >= rot_dims are copied.
 // Every token of a frame shares its angles, so a CTA (one frame of one head,
 // 64 tokens) forms the frame's cos/sin table once in shared memory.  One
-// 16-byte load and one 16-byte store per 8 channels: bound by HBM.
+// 16-byte load and one 16-byte store per 8 channels, a thread's loads all
+// issued before its stores: bound by HBM.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -39,22 +40,36 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const RopeParams p)
     const size_t base = (size_t)h * p.head_stride + (size_t)p.slot[f] * p.frame_stride;
     const int t0 = blockIdx.x * kRopeTokens;
     const int n_items = min(kRopeTokens, p.nf - t0) * chunks;
-    for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
-        const int t = t0 + it / chunks;
-        const int ch = it - (it / chunks) * chunks;
-        const size_t off = base + (size_t)t * p.d + ch * 8;
-        uint4 v = *reinterpret_cast<const uint4*>(p.src + off);
-        if (ch * 8 < p.rot_dims) {               // rot_dims is a multiple of 8
-            uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    // every load of the thread is issued before any store (bytes in flight)
+    constexpr int kPer = kRopeTokens * 16 / kRopeThreads;   // items per thread at d = 128
+    for (int i0 = threadIdx.x; i0 < n_items; i0 += kRopeThreads * kPer) {
+        uint4 v[kPer];
+        size_t off[kPer];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 r = cs[ch * 4 + k];
-                const float x0 = bf16_lo(w[k]), x1 = bf16_hi(w[k]);
-                w[k] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
-            }
-            v = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < kPer; ++k) {
+            const int it = i0 + k * kRopeThreads;
+            const int t = t0 + it / chunks;
+            const int ch = it - (it / chunks) * chunks;
+            off[k] = base + (size_t)t * p.d + ch * 8;
+            if (it < n_items) v[k] = *reinterpret_cast<const uint4*>(p.src + off[k]);
         }
-        *reinterpret_cast<uint4*>(p.dst + off) = v;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int it = i0 + k * kRopeThreads;
+            if (it >= n_items) break;
+            const int ch = it % chunks;
+            if (ch * 8 < p.rot_dims) {           // rot_dims is a multiple of 8
+                uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 r = cs[ch * 4 + j];
+                    const float x0 = bf16_lo(w[j]), x1 = bf16_hi(w[j]);
+                    w[j] = pack_bf16(x0 * r.x - x1 * r.y, x0 * r.y + x1 * r.x);
+                }
+                v[k] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            *reinterpret_cast<uint4*>(p.dst + off[k]) = v[k];
+        }
     }
 }
 
