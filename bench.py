@@ -64,6 +64,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The slowest rank's value (every rank gets it); x itself when ws == 1."""
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, ws: int, ms_slowest: float) -> float:
+    """Whole-job TFLOP/s: the work of all ws ranks over the slowest rank's time."""
+    return flops_per_rank_step * ws / (ms_slowest * 1e-3) / 1e12
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -515,11 +530,7 @@ def run_hf(args):
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     L.check_device_status()
     clocks = clk.summary()
-    ms = statistics.mean(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), ws, dev)
 
     # ---- per-kernel breakdown: the same step captured with event records between
     #      its kernels (external event nodes, so they time every replay) ----
@@ -569,9 +580,9 @@ def run_hf(args):
         for i in range(n_e2e):
             streamer.push(Qh, Kh, Vh, Oh[i % 2])
         streamer.synchronize()
-        e2e_ms = 1000 * (time.perf_counter() - t0) / n_e2e
+        e2e_ms = max_over_ranks(1000 * (time.perf_counter() - t0) / n_e2e, ws, dev)
         L2.check_device_status()
-        e2e = {"value": fl["total"] * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_throughput(fl["total"], ws, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": (streamer.h2d_bytes - b0) // n_e2e,
                "d2h_bytes_per_step": (streamer.d2h_bytes - d0) // n_e2e, "ms_per_step": e2e_ms,
                "how": "HostStreamer: per chunk, Q and the chunk's K/V copied from pinned host memory and O "
@@ -585,7 +596,7 @@ def run_hf(args):
     pk = peaks()
     attn_ms = statistics.mean(times["attention"])
     attn_tf = (fl["attn"] + fl["lin"]) / (attn_ms * 1e-3) / 1e12
-    value = fl["total"] * ws / (ms * 1e-3) / 1e12
+    value = job_throughput(fl["total"], ws, ms)
     per_kernel = {n: {"ms": statistics.mean(times[n])} for n in names}
     tot_k = sum(v["ms"] for v in per_kernel.values())
     for n in names:
