@@ -432,6 +432,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 misc[M_LAST] = 0;
                 misc[M_LAST + 1] = 0;
                 fence_mbar_init();
+                // the Q tiles depend only on the pair, so they load while the list is built
+                // (the previous pair's output store has finished reading the Q region)
+                const int ntiles = (nblk[0] > 0) + (nblk[1] > 0);
+                mbar_arrive_expect_tx(&bar[B_Q], ntiles * Cfg::G * Cfg::DCH * BETA * 128);
+                for (int t = 0; t < 2; ++t) {
+                    if (nblk[t] == 0) continue;
+                    uint8_t* sQ = smem + Cfg::OFF_Q + t * Cfg::Q_BYTES;
+                    for (int gq = 0; gq < Cfg::G; ++gq) {
+                        const int qb = qb0[t] + min(gq, nblk[t] - 1);   // missing blocks: reload the last one
+                        const int c = qb / g.bpf;
+                        const int j = qb - c * g.bpf;
+                        for (int m = 0; m < Cfg::DCH; ++m)
+                            tma_load_3d(sQ + m * (Cfg::TILE_M * 128) + gq * BETA * 128, &tmQ, &bar[B_Q], 64 * m,
+                                        j * BETA, bh * g.C + c);
+                    }
+                }
             }
             // ---- the pair's slab stream ----
             // mask bits of slab s: tile t, sub-block h (beta = 32 only), query
@@ -535,29 +551,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // list and barriers ready; a bad index: nothing of this pair is issued
-            if (bar_all_or(*wc.abort_flag != 0)) break;
+            // list and barriers ready; a bad index: nothing more of this pair is issued
+            // (the Q load in flight lands first)
+            if (bar_all_or(*wc.abort_flag != 0)) {
+                if (tid == 0) drain_wait(&bar[B_Q], 0, p.wait_limit_ns);
+                break;
+            }
             const int n_list = (int)misc[M_NLIST];
             const int n_rounds = (n_list + 1) / 2;
             rb = min(rb, n_rounds);
 
             if (warp == 0 && lane == 0) {
-                // ---------- Q tiles, key ring, state operand ----------
+                // ---------- key ring, state operand (Q was issued at the pair's start) ----------
                 bool ok = true;
-                const int ntiles = (nblk[0] > 0) + (nblk[1] > 0);
-                mbar_arrive_expect_tx(&bar[B_Q], ntiles * Cfg::G * Cfg::DCH * BETA * 128);
-                for (int t = 0; t < 2; ++t) {
-                    if (nblk[t] == 0) continue;
-                    uint8_t* sQ = smem + Cfg::OFF_Q + t * Cfg::Q_BYTES;
-                    for (int gq = 0; gq < Cfg::G; ++gq) {
-                        const int qb = qb0[t] + min(gq, nblk[t] - 1);   // missing blocks: reload the last one
-                        const int c = qb / g.bpf;
-                        const int j = qb - c * g.bpf;
-                        for (int m = 0; m < Cfg::DCH; ++m)
-                            tma_load_3d(sQ + m * (Cfg::TILE_M * 128) + gq * BETA * 128, &tmQ, &bar[B_Q], 64 * m,
-                                        j * BETA, bh * g.C + c);
-                    }
-                }
                 const int issued = produce_ring<D, BETA>(&tmK, sK, &bar[B_K_FULL], &bar[B_K_EMPTY], sList, n_list,
                                                          ra, rb, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
                 bool lin_issued = false;
@@ -1041,7 +1047,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok && !do_out) {
                         // another part finishes this pair; the MMA thread still waits for phi(Q)
                         mbar_arrive(&bar[B_PHIQ + t]);
-                    } else if (ok) {
+                    } else if (ok && (participated ||
+                                      __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_Q], 0, wc, SITE_ATTN_Q)))) {
+                        // (a tile that took part in no round of this part waits for its Q tile
+                        // here; otherwise its S_FULL waits already covered the Q load)
                         tc_fence_after();
                         // phi(q) (bf16, in place over Q) and the linear-read denominator.  The
                         // row is loaded whole, transformed in registers (z read alongside, four
