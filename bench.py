@@ -386,7 +386,9 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
       (W = 21 frames, every key block selected, empty state: the method's own
       dense special case), same chunk, same kernels.
     - rope_prestep: the relative temporal RoPE pre-step on the chunk's
-      queries and the window's keys (HBM-bound)."""
+      queries and the window's keys (HBM-bound).
+    - long_horizon: the 240-frame stream through the layer, step times in
+      buckets of 10 steps (flat when the state's cost does not grow)."""
     from hybrid_sparse_linear_scores_b300 import binding as hb
     from hybrid_sparse_linear_scores_b300 import synth
     from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, frames_tensor
@@ -448,6 +450,42 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
                             "how": "hf_hybrid_forward_ex (cached key pools) with topk = all blocks and S = z = 0, "
                                    "one CUDA graph, L2 flushed before each replay"}
     del Ld
+
+    # long horizon: the 240-frame stream (80 chunks) through the layer's own
+    # step (absorb of the evicted frames, ring write + key pooling, forward);
+    # every step timed, medians per 10-step bucket should be flat
+    from hybrid_sparse_linear_scores_b300.stream import HybridAttentionLayer
+    w3 = CONFIGS["stream"]
+    cfg3 = hb.make_config(w3.batch, w3.heads, w3.head_dim, w3.tokens_per_frame, w3.window_frames,
+                          w3.chunk_frames, w3.block_size, w3.k_for(w3.steps - 1))
+    L3 = HybridAttentionLayer(cfg3, dev)
+    state_bytes = {L3.S.numel() * 4 + L3.z.numel() * 4}
+    per_step = []
+    for st in range(w3.steps):
+        L3.cfg.topk = w3.k_for(st)
+        Kn = frames_tensor(w3, synth.STREAM_K, w3.chunk(st), dev)
+        Vn = frames_tensor(w3, synth.STREAM_V, w3.chunk(st), dev)
+        Q3 = frames_tensor(w3, synth.STREAM_Q, w3.chunk(st), dev).reshape(w3.heads_total, -1, w3.head_dim)
+        O3 = torch.empty_like(Q3)
+        idx3 = torch.empty((w3.heads_total, w3.n_qb(), w3.k_for(st)), dtype=torch.int32, device=dev)
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        L3.step(Q3, Kn, Vn, O3, idx3)
+        e1.record()
+        torch.cuda.synchronize()
+        per_step.append(e0.elapsed_time(e1))
+        state_bytes.add(L3.S.numel() * 4 + L3.z.numel() * 4)
+    L3.check_device_status()
+    buckets = [statistics.median(per_step[i:i + 10]) for i in range(0, len(per_step), 10)]
+    out["long_horizon"] = {"workload": f"{w3.name}: {w3.steps} chunks of {w3.chunk_frames} frames "
+                                       f"(b{w3.batch} H{w3.heads} d{w3.head_dim} N_f{w3.tokens_per_frame} "
+                                       f"W{w3.window_frames} beta{w3.block_size}, K = 25 % of the window)",
+                           "bucket_median_ms_per_step": buckets,
+                           "state_bytes": sorted(state_bytes),
+                           "how": "layer.step per chunk (absorb, ring write + key pooling, forward), eager "
+                                  "launches, CUDA events around each step, L2 flushed before each"}
+    del L3
     return out
 
 
@@ -613,6 +651,8 @@ def run_hf(args):
                              "the new chunk, hybrid forward with cached key pools: 6 kernels)",
                    "parallelism": f"replicas x{ws}"},
         "us_per_latent_frame": 1000 * ms / w.chunk_frames,
+        "median_ms_per_step": statistics.median(step_ms),
+        "median_us_per_latent_frame": 1000 * statistics.median(step_ms) / w.chunk_frames,
         "pct_bf16_peak": 100 * value / pk["bf16_tflops"],
         "warm_l2_ms_per_step": warm_ms,
         "flops_per_step": fl, "bytes_per_step": by,
