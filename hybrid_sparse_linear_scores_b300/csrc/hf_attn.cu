@@ -33,10 +33,11 @@
 // not depend on the order of arrival -- and runs the epilogue.
 //
 // Warp roles (384 threads = 3 warpgroups, 1 CTA per SM):
-//   warps 0-3  build the pair's slab stream; then
-//   warp 0     TMA producer of the Q tiles, of the keys (a ring of NR round
-//              stages) and, at the end, of the bf16 hi/lo state S for the
-//              fused linear read (into the key ring);
+//   warps 0-3  build the pair's slab stream (thread 0 issues the Q tiles'
+//              loads first: they depend only on the pair); then
+//   warp 0     TMA producer of the keys (a ring of NR round stages) and, at
+//              the end, of the bf16 hi/lo state S for the fused linear read
+//              (into the key ring);
 //   warp 2     TMA producer of the values (a second ring of NR round stages).
 //              Keys are released as soon as Q K^T has read them, values
 //              after P V: each ring runs about NR rounds ahead.
