@@ -629,7 +629,15 @@ def run_hf(args):
 
     extra = {}
     if not args.skip_extras:
-        extra = extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush, ms, args)
+        # secondary figures: a failure there is reported in the line, not allowed to
+        # take the step's own measurement with it
+        try:
+            extra = extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush, ms, args)
+        except Exception as exc:   # noqa: BLE001 - reported, not swallowed
+            print(f"bench: extra measurements failed: {exc!r}", file=sys.stderr, flush=True)
+            extra = {"extras_error": repr(exc)}
+        torch.cuda.synchronize()
+        L.check_device_status()
 
     pk = peaks()
     attn_ms = statistics.mean(times["attention"])
