@@ -328,7 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool split = p.pair_rounds != nullptr;
     uint32_t T = 0, s_c = 0, e_c = 0;
     if (split) {
-        int* tsum = reinterpret_cast<int*>(sK);   // [kThreads]: the key ring is free before the first pair
+        // [kThreads] scratch in the slab list, which only ever sees ordinary loads and
+        // stores (TMA never writes it) and is first filled by the first pair's list
+        int* tsum = reinterpret_cast<int*>(sList);
+        static_assert(Cfg::MAX_SLABS >= kThreads, "the prologue's scratch fits in the slab list");
         const int NP = p.total_pairs;
         const int per = (NP + kThreads - 1) / kThreads;
         const int b0 = min(NP, tid * per), b1 = min(NP, b0 + per);
