@@ -141,3 +141,23 @@ def test_rope_argument_errors_are_synchronous(kw, msg):
                             a["max_offset"], a["rot_dims"], a["theta_base"], stream=0)
     assert ei.value.code == 1
     assert msg in str(ei.value)
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(Kc=0), "Kc is NULL"), (dict(ws=FAKE + 8), "ws is not 16-byte aligned"),
+    (dict(slots=[0, 0]), "given twice"), (dict(slots=[9]), "outside"), (dict(slots=[-1]), "outside"),
+    (dict(slot_stride=100), "slot_stride"), (dict(slots=list(range(10))), "n_slots"),
+])
+def test_pool_keys_argument_errors_are_synchronous(kw, msg):
+    cfg = cfg_of(CONFIGS["realistic"])
+    a = dict(Kc=FAKE, slot_stride=cfg.tokens_per_frame, slots=[0, 1, 2], ws=FAKE)
+    a.update(kw)
+    with pytest.raises(hb.HFError) as ei:
+        hb.hf_pool_keys(cfg, a["Kc"], a["slot_stride"], a["slots"], a["ws"], stream=0)
+    assert ei.value.code == 1
+    assert msg in str(ei.value)
+
+
+def test_pool_keys_of_no_slot_is_a_no_op():
+    cfg = cfg_of(CONFIGS["realistic"])
+    hb.hf_pool_keys(cfg, FAKE, cfg.tokens_per_frame, [], FAKE, stream=0)
