@@ -293,7 +293,7 @@ hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_
     float* qp = reinterpret_cast<float*>(w + L.qp);
     float* kp = reinterpret_cast<float*>(w + L.kp);
     HF_LAUNCH(launch_pool(Q, Kc, g, window_frames(sm, n_win), qp, kp, stream), "pool launch");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, nullptr, stream), "score launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, nullptr, nullptr, stream), "score launch");
     return HF_OK;
 }
 
@@ -402,7 +402,7 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
     HF_LAUNCH(mark(0), "event record");
     HF_LAUNCH(launch_pool(Q, Kc, g, pf, qp, kp, stream), "pool launch");
     HF_LAUNCH(mark(1), "event record");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, prounds, stream), "score/select launch");
+    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, prounds, counters, stream), "score/select launch");
     HF_LAUNCH(mark(2), "event record");
     HF_LAUNCH(launch_smma_prep(S, g, smma, stream), "state prep launch");
     HF_LAUNCH(mark(3), "event record");

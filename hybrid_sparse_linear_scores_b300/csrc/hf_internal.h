@@ -87,8 +87,10 @@ constexpr int kAttnMaxGrid = 160;
 // ---- launchers (return cudaError_t as int) --------------------------------
 int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* qp, float* kpc,
                 void* stream);
+// pair_rounds (optional): rounds of each tile pair's slab stream for the attention
+// kernel's balancing; with it, counters (the pairs' arrival counters) are zeroed.
 int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                        int32_t* idx, int32_t* pair_rounds, void* stream);
+                        int32_t* idx, int32_t* pair_rounds, uint32_t* counters, void* stream);
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
 int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
                 const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,

@@ -53,13 +53,13 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const uint16_t* __re
     constexpr int TASKS = kPoolThreads / TPB;
     constexpr int ROW = D / 8;   // uint4 per token row
     extern __shared__ __align__(16) uint4 stage[];   // [beta rows][kPoolThreads]
-    const int task = blockIdx.x * TASKS + threadIdx.x / TPB;
+    const int64_t task = (int64_t)blockIdx.x * TASKS + threadIdx.x / TPB;
     const int part = threadIdx.x % TPB;
     const int nq = pf.with_q ? g.nqb : 0;
     const int per_head = nq + pf.n * g.bpf;
-    if (task >= g.BH * per_head) return;
-    const int bh = task / per_head;
-    const int b = task - bh * per_head;
+    if (task >= (int64_t)g.BH * per_head) return;
+    const int bh = (int)(task / per_head);
+    const int b = (int)(task - (int64_t)bh * per_head);
 
     const uint16_t* src;
     int j;
@@ -192,7 +192,8 @@ struct ScoreSmem {
 template <int D, bool WRITE_SCORES, bool SELECT>
 __global__ void __launch_bounds__(256) score_select_kernel(const float* __restrict__ qp, const float* __restrict__ kpc,
                                                            Geom g, SlotMap sm, float* __restrict__ scores,
-                                                           int32_t* __restrict__ idx, int32_t* __restrict__ pair_rounds)
+                                                           int32_t* __restrict__ idx, int32_t* __restrict__ pair_rounds,
+                                                           uint32_t* __restrict__ counters)
 {
     extern __shared__ __align__(16) float smf[];
     float* qps = smf;
@@ -294,7 +295,14 @@ __global__ void __launch_bounds__(256) score_select_kernel(const float* __restri
             int cnt = 0;
             for (int i = lane; i < words; i += 32) cnt += __popc(bits[warp * words + i]);
             cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
-            if (lane == 0) pair_rounds[(size_t)bh * pairs_per_head + pair0 + warp] = (cnt + 1) / 2;
+            if (lane == 0) {
+                const size_t pair = (size_t)bh * pairs_per_head + pair0 + warp;
+                pair_rounds[pair] = (cnt + 1) / 2;
+                // the attention kernel that follows counts the parts of a split pair
+                // here; a launch that gave up part-way can leave a count behind
+                counters[2 * pair] = 0u;
+                counters[2 * pair + 1] = 0u;
+            }
         }
     }
 }
@@ -346,29 +354,30 @@ int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const Pool
 
 template <int D, bool W, bool S>
 static int launch_score_t(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                          int32_t* idx, int32_t* pair_rounds, cudaStream_t st)
+                          int32_t* idx, int32_t* pair_rounds, uint32_t* counters, cudaStream_t st)
 {
     auto k = score_select_kernel<D, W, S>;
     cudaError_t e = set_smem(k, ScoreSmem<D>::bytes);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + QG - 1) / QG;
-    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kpc, g, sm, scores, idx, pair_rounds);
+    k<<<g.BH * groups, 256, ScoreSmem<D>::bytes, st>>>(qp, kpc, g, sm, scores, idx, pair_rounds, counters);
     return (int)cudaGetLastError();
 }
 
 int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                        int32_t* idx, int32_t* pair_rounds, void* stream)
+                        int32_t* idx, int32_t* pair_rounds, uint32_t* counters, void* stream)
 {
+    if (pair_rounds && !counters) return (int)cudaErrorInvalidValue;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool w = scores != nullptr, s = idx != nullptr;
     if (g.d == 128) {
-        if (w && s) return launch_score_t<128, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
-        if (w) return launch_score_t<128, true, false>(qp, kpc, g, sm, scores, idx, nullptr, st);
-        return launch_score_t<128, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
+        if (w && s) return launch_score_t<128, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, counters, st);
+        if (w) return launch_score_t<128, true, false>(qp, kpc, g, sm, scores, idx, nullptr, nullptr, st);
+        return launch_score_t<128, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, counters, st);
     }
-    if (w && s) return launch_score_t<64, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
-    if (w) return launch_score_t<64, true, false>(qp, kpc, g, sm, scores, idx, nullptr, st);
-    return launch_score_t<64, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, st);
+    if (w && s) return launch_score_t<64, true, true>(qp, kpc, g, sm, scores, idx, pair_rounds, counters, st);
+    if (w) return launch_score_t<64, true, false>(qp, kpc, g, sm, scores, idx, nullptr, nullptr, st);
+    return launch_score_t<64, false, true>(qp, kpc, g, sm, scores, idx, pair_rounds, counters, st);
 }
 
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream)

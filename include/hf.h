@@ -106,11 +106,13 @@ HF_API const char *hf_last_error(void);
  * concurrently need separate workspaces.  Calls that share one may differ
  * in topk (up to cfg->topk of the sizing call) and in the window, not in the
  * other fields.  It must be zeroed once before first use (its first 256
- * bytes are the device status word; counters of the attention kernel's split
- * pairs follow, which every completed call leaves at zero; after a call that
- * reported an error, zero the workspace again).  It also holds the
- * pooled-key cache of the layer's ring (see hf_pool_keys): one workspace per
- * ring. */
+ * bytes are the device status word, read and cleared by
+ * hf_get_device_status).  The counters that the attention kernel keeps for
+ * tile pairs it splits between CTAs follow; every forward resets them before
+ * its attention kernel runs, so a call that gave up part-way (a device
+ * error) leaves nothing behind that changes a later call.  The workspace
+ * also holds the pooled-key cache of the layer's ring (see hf_pool_keys):
+ * one workspace per ring. */
 HF_API hf_status hf_workspace_size(const hf_config *cfg, size_t *bytes /* host */);
 
 /* S = 0, z = 0 (the empty state). */
@@ -304,7 +306,10 @@ HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t
  *     device, which must be the device of `stream` and of the buffers) looks
  *     up the array's device address with cudaGetSymbolAddress, which may load
  *     the library's module on that device.  Make that first call before any
- *     stream capture.  Later calls on the device reuse the address.
+ *     stream capture.  Later calls on the device reuse the address for the
+ *     rest of the process.  A cudaDeviceReset (or anything else that destroys
+ *     the device's primary context) can move the array: do not call this
+ *     entry point on that device after such a reset in the same process.
  *   - Sharing: every call on a device uses the same array, and the array
  *     keeps whatever the last call left in it.  All of it is rewritten before
  *     it is read except the status word, which starts at zero when the

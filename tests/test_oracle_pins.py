@@ -160,6 +160,78 @@ def test_topk_rejects_bad_k_and_nonfinite():
 
 
 # --------------------------------------------------------------------------
+# near-tie margin report (English technical summary, section 2.A.2: the
+# top-K blocks by importance score; the margin between the K-th and the
+# (K+1)-th score says how close a selection is to a tie)
+# --------------------------------------------------------------------------
+def test_score_margin_hand_derived():
+    """Scores {5, 3, 3, 1} (d = 1): K = 1 -> 5 - 3 = 2, K = 2 -> 3 - 3 = 0,
+    K = 3 -> 3 - 1 = 2, K = nKB -> 0 by definition.  Catches an off-by-one in
+    the rank (the K-th and (K+1)-th largest)."""
+    qp = np.array([[1.0]], np.float32)
+    kp = np.array([[5.0], [3.0], [3.0], [1.0]], np.float32)
+    got = [float(oracle.score_margin(qp, kp, k)[0]) for k in (1, 2, 3, 4)]
+    assert got == [2.0, 0.0, 2.0, 0.0]
+
+
+def test_score_margin_rows_and_operand_layout():
+    """Two query blocks, d = 2.  Row 0: q = (1, 2) against k = (1, 2), (2, 1),
+    (0, 0) scores 5, 4, 0; row 1: q = (2, 0) scores 2, 4, 0.  K = 1 gives
+    margins 1 and 2; K = 2 gives 4 and 2.  Catches a transposed key matrix
+    (k read channel-major) and a row mix-up (margins of row 0 written to row 1)."""
+    qp = np.array([[1.0, 2.0], [2.0, 0.0]], np.float32)
+    kp = np.array([[1.0, 2.0], [2.0, 1.0], [0.0, 0.0]], np.float32)
+    np.testing.assert_array_equal(oracle.score_margin(qp, kp, 1), [1.0, 2.0])
+    np.testing.assert_array_equal(oracle.score_margin(qp, kp, 2), [4.0, 2.0])
+
+
+def test_score_margin_is_double_precision():
+    """q = (1, 1), k0 = (2^24, 1), k1 = (2^24, 0): the scores 2^24 + 1 and 2^24
+    are equal in float32 but not in float64, so the K = 1 margin is exactly 1.
+    Catches a margin taken from the float32 scores."""
+    qp = np.array([[1.0, 1.0]], np.float32)
+    kp = np.array([[2.0 ** 24, 1.0], [2.0 ** 24, 0.0]], np.float32)
+    assert float(oracle.score_margin(qp, kp, 1)[0]) == 1.0
+    s32 = oracle.scores(qp, kp)
+    assert s32[0, 0] == s32[0, 1]
+
+
+@pytest.mark.parametrize("name", ["sweep_k10_b64", "sweep_k25_b128", "realistic"])
+def test_score_margin_against_sorted_double_scores(name):
+    """On a full-size workload (clustered keys: the near-tie stress), every
+    query block's margin equals the gap between the K-th and (K+1)-th largest
+    of the float64 scores computed here by a matrix product and a sort; and
+    wherever the float32 selection differs from the float64 ranking, the
+    margin is below the float32 rounding error of the scores.  Reports the
+    smallest margin seen."""
+    from hybrid_sparse_linear_scores_b300.workloads import SWEEP
+    w = CONFIGS.get(name) or next(s for s in SWEEP if s.name == name)
+    Q = frames_tensor(w, synth.STREAM_Q, w.chunk(0))
+    K = frames_tensor(w, synth.STREAM_K, w.window(0))
+    k = w.k_for(0)
+    smallest, flips = math.inf, 0
+    for h in (0, w.heads_total // 2, w.heads_total - 1):
+        qp = oracle.pool(Q[h], w.block_size)
+        kp = oracle.pool(K[h], w.block_size)
+        m = oracle.score_margin(qp, kp, k)
+        s64 = qp.astype(np.float64) @ kp.astype(np.float64).T
+        desc = -np.sort(-s64, axis=1)
+        np.testing.assert_allclose(m, desc[:, k - 1] - desc[:, k], rtol=1e-9, atol=1e-9 * np.abs(desc).max())
+        sel32 = oracle.topk(oracle.scores(qp, kp), k)
+        # float32 score error bound: d products and adds, each within 2^-24 of
+        # the exact value of |q_c k_c| summed
+        bound = (qp.shape[1] + 1) * 2.0 ** -24 * (np.abs(qp).astype(np.float64) @ np.abs(kp).astype(np.float64).T)
+        for r in range(qp.shape[0]):
+            top64 = set(np.argsort(-s64[r], kind="stable")[:k])
+            if top64 != set(sel32[r]):
+                flips += 1
+                assert m[r] <= 2 * bound[r].max(), (r, m[r], bound[r].max())
+        smallest = min(smallest, float(m.min()))
+    print(f"{name}: smallest float64 margin between ranks K and K+1: {smallest:.3e}; "
+          f"query blocks whose float32 selection differs from the float64 ranking: {flips}")
+
+
+# --------------------------------------------------------------------------
 # attention: reductions to textbook cases
 # --------------------------------------------------------------------------
 def dense_window_attention(q, k, v, scale):
@@ -228,6 +300,73 @@ def test_key_permutation_within_frame_invariance():
     a = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=nkb)["O"]
     b = oracle.hybrid_forward(Q, Kp, Vp, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=nkb)["O"]
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def _block_table(n_frames, nf, beta):
+    """(frame, first token, end token) of every block, built by walking each
+    frame's tokens (not from a closed-form index)."""
+    blocks = []
+    for f in range(n_frames):
+        t = 0
+        while t < nf:
+            blocks.append((f, t, min(t + beta, nf)))
+            t += beta
+    return blocks
+
+
+def masked_sparse_attention(q, k, v, C, nf, beta, idx, scale):
+    """Block-sparse attention as a dense masked softmax: row i of the chunk may
+    see key token t only if t's block is in the selection of i's block."""
+    qblocks = _block_table(C, nf, beta)
+    kblocks = _block_table(k.shape[0] // nf, nf, beta)
+    row_block = np.empty(C * nf, np.int64)
+    for b, (f, t0, t1) in enumerate(qblocks):
+        row_block[f * nf + t0:f * nf + t1] = b
+    key_block = np.empty(k.shape[0], np.int64)
+    for b, (f, t0, t1) in enumerate(kblocks):
+        key_block[f * nf + t0:f * nf + t1] = b
+    allowed = np.zeros((C * nf, k.shape[0]), bool)
+    for i in range(C * nf):
+        allowed[i] = np.isin(key_block, idx[row_block[i]])
+    l = scale * (q.double().numpy() @ k.double().numpy().T)
+    l = np.where(allowed, l, -np.inf)
+    l -= l.max(axis=1, keepdims=True)
+    p = np.exp(l)
+    return (p @ v.double().numpy()) / p.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("nf,beta,C,n_win,kk", [(10, 4, 2, 3, 3), (7, 3, 3, 4, 2), (9, 9, 2, 2, 1)])
+def test_sparse_attn_is_masked_dense_softmax(nf, beta, C, n_win, kk):
+    """oracle.sparse_attn with a selection drawn at random per query block
+    (different blocks select different keys) against a dense softmax masked
+    by the selection.  Rows straddle a frame's ragged last block and the
+    boundary between frames.  Catches a wrong row -> query-block mapping
+    (flat tiling across frames, a missing frame term), a wrong key-block ->
+    token range, and a row subset that returns the wrong rows."""
+    d = 8
+    q = rnd((C * nf, d), 40)
+    k = rnd((n_win * nf, d), 41)
+    v = rnd((n_win * nf, d), 42)
+    nqb = C * -(-nf // beta)
+    nkb = n_win * -(-nf // beta)
+    rng = np.random.default_rng(nf + beta)
+    idx = np.stack([np.sort(rng.choice(nkb, size=kk, replace=False)) for _ in range(nqb)]).astype(np.int32)
+    scale = 1 / math.sqrt(d)
+    ref = masked_sparse_attention(q, k, v, C, nf, beta, idx, scale)
+    got = oracle.sparse_attn(q, k, v, C, nf, beta, idx)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    rows = [nf - 2, nf - 1, nf, nf + 1, C * nf - 1]
+    np.testing.assert_array_equal(oracle.sparse_attn(q, k, v, C, nf, beta, idx, rows=rows), got[rows])
+
+
+def test_sparse_attn_matches_the_forward_split():
+    """The standalone sparse attention with the forward's own selection
+    reproduces the forward's softmax path (O_swa)."""
+    nf, beta, C, n_win, d = 10, 4, 2, 3, 8
+    Q, K, V = rnd((1, C * nf, d), 43), rnd((1, n_win * nf, d), 44), rnd((1, n_win * nf, d), 45)
+    out = oracle.hybrid_forward(Q, K, V, None, None, C=C, n_win=n_win, nf=nf, beta=beta, k=4, split=True)
+    got = oracle.sparse_attn(Q[0], K[0], V[0], C, nf, beta, out["idx"][0])
+    np.testing.assert_allclose(got, out["O_swa"][0], rtol=1e-14, atol=1e-15)
 
 
 # --------------------------------------------------------------------------
