@@ -175,7 +175,8 @@ def hf_hybrid_forward(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx
 
 def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, events,
                                stream=None):
-    """events: 5 torch.cuda.Event objects (recorded between the kernels).
+    """events: HF_FWD_EVENTS (4) torch.cuda.Event objects (before the key
+    pooling, before the prologue, before the attention kernel, after it).
     torch creates an event's CUDA handle on its first record and only
     reports times for events it has recorded, so each event is recorded by
     torch first; the library then records it again at its own point."""
@@ -186,13 +187,14 @@ def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, 
         if e is not None:
             e.record(ts)
     sm = _slots(slot_map)
-    ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
+    ev = (ctypes.c_void_p * HF_FWD_EVENTS)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
     _check(lib().hf_hybrid_forward_profiled(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride),
                                             sm and sm[0], int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out),
                                             _ptr(ws), st, ev), "hf_hybrid_forward_profiled")
 
 
 HF_FWD_CACHED_KEYS = 1
+HF_FWD_EVENTS = 4
 
 
 def hf_pool_keys(cfg, Kc, slot_stride, slots, ws, stream=None):
@@ -229,7 +231,7 @@ def hf_rope_relative(cfg, src, dst, head_stride, frame_stride, slots, offsets, m
 def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, flags=0, events=None,
                          stream=None):
     """hf_hybrid_forward with flags (HF_FWD_CACHED_KEYS) and optional per-kernel
-    events (5 torch.cuda.Event objects, handled as in hf_hybrid_forward_profiled)."""
+    events (HF_FWD_EVENTS torch.cuda.Event objects, handled as in hf_hybrid_forward_profiled)."""
     st = _stream(stream)
     ev = None
     if events is not None:
@@ -238,7 +240,7 @@ def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, 
         for e in events:
             if e is not None and not e.cuda_event:   # torch creates the CUDA event on its first record
                 e.record(ts)
-        ev = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
+        ev = (ctypes.c_void_p * HF_FWD_EVENTS)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
     sm = _slots(slot_map)
     _check(lib().hf_hybrid_forward_ex(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride), sm and sm[0],
                                       int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out), _ptr(ws), st,

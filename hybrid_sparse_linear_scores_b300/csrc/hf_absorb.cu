@@ -5,29 +5,43 @@
 //   S[c][j] += sum_t phi(k_t[c]) v_t[j],   z[c] += sum_t phi(k_t[c]).
 //
 // Per head this is a [d x n] x [n x d] GEMM contracted over the n evicted
-// tokens: tcgen05 with M = 128 (phi features; zero-padded when d = 64),
-// N = d (value channels), both operands MN-major straight from the TMA tiles.
-// phi(k) enters the MMA as a bf16 pair hi + lo (hi = rn(phi), lo =
-// rn(phi - hi)), two MMAs into one fp32 accumulator, so S keeps ~16 bits
-// more than a bf16 operand would give; z is summed in fp32 on CUDA cores.
-// The tensor-core accumulator only ever holds one 64-token tile: two TMEM
-// accumulators alternate, and the epilogue warps fold each finished tile
-// into fp32 registers with round-to-nearest adds while the next tile is
-// multiplied, so long absorbs do not accumulate the tensor core's internal
-// rounding over thousands of steps.
+// tokens, with about 64 FLOP per byte read: the bound is HBM bandwidth, so the
+// design is about keeping every SM streaming.
 //
-// One thread-block cluster (CL <= 8 CTAs) per head splits the tokens; the
-// CL partial states are summed through distributed shared memory in rank
-// order, then added to S in global memory: deterministic, no atomics, no
-// partial states in HBM.
+// Work split.  A head's value channels are cut into NG column groups of NV
+// channels (NG = d / NV), and each (head, column group) is one thread-block
+// cluster of CL CTAs that split the tokens; the host picks NG and CL so that
+// all clusters are resident at once (occupancy query) and the CTAs cover the
+// SMs.  Every CTA reads all d key channels of its tokens (phi needs them) and
+// the NV value channels of its group; a key tile read by both groups of a
+// head comes from L2 the second time.
+//
+// Per 64-token tile: TMA brings the key tile (d channels) and the value tile
+// (NV channels) into a stage of a ring of 6-8 stages.  The transform warps compute
+// phi(k) for one feature per thread and write it straight into tensor memory
+// as the MMA's A operand, as a bf16 pair hi = rn(phi), lo = rn(phi - hi)
+// (about 16 significant bits, twice a bf16 operand's); z is summed on the
+// way, in float32.  The MMA warp then runs D = phi(K)^T V with A from tensor memory
+// and B = the value tile in shared memory (hi and lo: two MMA chains into one
+// accumulator), M = 128 features (zero rows when d = 64), N = NV.  The tensor
+// core only ever accumulates one tile: two accumulators alternate, and the
+// transform warps fold each finished tile into float32 registers with
+// round-to-nearest adds while the next one is multiplied.
+//
+// The CL partial states of a cluster are summed through distributed shared
+// memory in rank order and added to S in global memory (no atomics, no
+// partial states in HBM): results are deterministic for a given launch shape.
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 2-9 phi transform (in place over the K tile) and epilogue.
+// issuer, warps 2-9 phi transform and accumulator folding (feature 32q + lane
+// of the warp's TMEM lane quarter q; warps 2-5 take the first 32 tokens of a
+// tile and the first half of the accumulator's columns, warps 6-9 the rest).
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "hf_internal.h"
 #include "hf_ptx.cuh"
@@ -37,145 +51,177 @@ namespace cg = cooperative_groups;
 namespace hf {
 namespace {
 
-template <int D>
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+template <int D, int NV>
 struct AbsCfg {
-    static constexpr int TT = 64;                    // tokens per tile (MMA K extent per tile)
-    static constexpr int NS = 4;                     // stages
-    static constexpr int CHUNK = TT * 128;           // one 64-column chunk of a tile: 8 KB
-    static constexpr int OFF_K = 0;                  // 2 chunks (chunk 1 zero when D = 64)
-    static constexpr int OFF_LO = 2 * CHUNK;         // 2 chunks
-    static constexpr int OFF_V = 4 * CHUNK;          // D/64 chunks
-    static constexpr int STAGE = OFF_V + (D / 64) * CHUNK;
-    static constexpr int OFF_MISC = NS * STAGE;
-    static constexpr int NBAR = 20;
-    static_assert(NS <= 4, "barrier slots hold at most 4 stages");
-    static constexpr int OFF_ZP = OFF_MISC + 64 + 8 * NBAR;   // fp32 [8][D] z partials
-    static constexpr uint32_t TMEM_COLS = 256;                 // two accumulators of 128 columns
-    static constexpr int SMEM = OFF_ZP + 8 * D * 4;
-    static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static constexpr int PITCH = D + 4;              // partial-state row pitch (floats; rows 16-byte aligned)
-    static_assert(128 * PITCH * 4 <= NS * STAGE, "partial state must fit in the stage buffers");
-    static constexpr uint32_t IDESC = idesc_bf16_f32(128, D, true, true);
-    static constexpr int NTHR = 320;
+    static constexpr int TT = 64;                    // tokens per tile
+    static constexpr int CHUNK = TT * 128;           // 64 channels x 64 tokens, 128-byte swizzle: 8 KB
+    static constexpr int K_BYTES = (D / 64) * CHUNK;
+    static constexpr int V_BYTES = (NV / 64) * CHUNK;
+    static constexpr int STAGE = K_BYTES + V_BYTES;
+    static constexpr int NS = STAGE <= 24 * 1024 ? 8 : 6;   // shared-memory stages (tiles in flight)
+    static constexpr int NA = 4;                     // TMEM A-operand stages
+    static constexpr int TW = 16;                    // transform warps: 4 per TMEM lane quarter
+    static constexpr int TPW = TT / 4;               // tokens of a tile per transform warp
+    static constexpr int NC = NV / 4;                // accumulator columns folded per transform warp
+    static constexpr int PITCH = NV + 4;             // partial-state row pitch (floats; rows 16-byte aligned)
+    static constexpr int PART_BYTES = 128 * PITCH * 4;
+    static constexpr int BUF = cmax(NS * STAGE, PART_BYTES);
+    static constexpr int OFF_BAR = BUF;              // mbarriers: FULL[NS], EMPTY[NS], PHI[NA], ACC_FULL[2], ACC_FREE[2], DRAIN
+    static constexpr int NBAR = 2 * NS + NA + 5;
+    static constexpr int OFF_MISC = OFF_BAR + 8 * 32;             // uint32 [16]
+    static constexpr int OFF_ZP = OFF_MISC + 64;                  // fp32 [4][128] z partials (token quarters)
+    static constexpr int SMEM = OFF_ZP + 4 * 128 * 4;
+    // more than half of an SM's shared memory: one CTA per SM, so that its
+    // 512 TMEM columns are always free when it starts
+    static constexpr int SMEM_ALLOC = cmax(SMEM + 1024, 116 * 1024);
+    static constexpr uint32_t A_COLS = 64;           // per A stage: hi [0, 32), lo [32, 64)
+    static constexpr uint32_t ACC0 = NA * A_COLS;    // accumulators at ACC0 + b * NV
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(ACC0 + 2 * NV <= TMEM_COLS, "TMEM budget");
+    static_assert(NBAR <= 32, "barrier slots");
+    static_assert(NS >= NA, "a TMEM stage is rewritten only after its MMA completed");
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, NV, false, true);   // A from TMEM, B MN-major
+    static constexpr int NTHR = 32 * (2 + TW);
+    static constexpr int B_FULL = 0, B_EMPTY = NS, B_PHI = 2 * NS, B_ACC_FULL = 2 * NS + NA,
+                         B_ACC_FREE = B_ACC_FULL + 2, B_DRAIN = B_ACC_FREE + 2;
 };
 
-// barrier slots: A_FULL, A_PHI, A_EMPTY have one per stage (NS <= 4)
-enum { A_FULL = 0, A_PHI = 4, A_EMPTY = 8, A_ACC_FULL = 12, A_ACC_FREE = 14, A_DRAIN = 16 };
+// misc words
+enum { X_TMEM = 0, X_ABORT = 1 };
 
 struct AbsParams {
-    int BH, n, CL;
+    int BH, n, NG, CL;
     float* S;
     float* z;
     uint32_t* status;
     uint64_t wait_limit_ns;
 };
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int NV>
+__global__ void __launch_bounds__(AbsCfg<D, NV>::NTHR, 1)
     absorb_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AbsParams p)
 {
-    using Cfg = AbsCfg<D>;
+    using Cfg = AbsCfg<D, NV>;
+    constexpr int NS = Cfg::NS, NA = Cfg::NA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);      // [0] tmem, [1] abort
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_MISC + 64);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     float* zp = reinterpret_cast<float*>(smem + Cfg::OFF_ZP);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
-    const int bh = blockIdx.x / p.CL;
+    const int cid = blockIdx.x / p.CL;                 // cluster = (head, column group)
+    const int bh = cid / p.NG;
+    const int grp = cid - bh * p.NG;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n_tiles = (p.n + Cfg::TT - 1) / Cfg::TT;
     const int t_begin = (int)((long)rank * n_tiles / p.CL);
     const int t_end = (int)((long)(rank + 1) * n_tiles / p.CL);
     const int my_tiles = t_end - t_begin;
 
-    WaitCtl wc{reinterpret_cast<volatile uint32_t*>(misc + 1), p.status, p.wait_limit_ns};
+    WaitCtl wc{reinterpret_cast<volatile uint32_t*>(misc + X_ABORT), p.status, p.wait_limit_ns};
 
     if (tid == 0) {
-        for (int s = 0; s < Cfg::NS; ++s) {
-            mbar_init(&bar[A_FULL + s], 1);
-            mbar_init(&bar[A_PHI + s], 256);
-            mbar_init(&bar[A_EMPTY + s], 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&bar[Cfg::B_FULL + s], 1);
+            mbar_init(&bar[Cfg::B_EMPTY + s], 1);
         }
+        for (int s = 0; s < NA; ++s) mbar_init(&bar[Cfg::B_PHI + s], 32 * Cfg::TW);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&bar[A_ACC_FULL + b], 1);
-            mbar_init(&bar[A_ACC_FREE + b], 256);
+            mbar_init(&bar[Cfg::B_ACC_FULL + b], 1);
+            mbar_init(&bar[Cfg::B_ACC_FREE + b], 32 * Cfg::TW);
         }
-        mbar_init(&bar[A_DRAIN], 1);
-        misc[1] = 0;
+        mbar_init(&bar[Cfg::B_DRAIN], 1);
+        misc[X_ABORT] = 0;
         fence_mbar_init();
     }
-    if (D == 64) {   // the zero halves of the M = 128 operands
-        for (int s = 0; s < Cfg::NS; ++s)
-            for (int i = tid; i < Cfg::CHUNK / 16; i += Cfg::NTHR) {
-                reinterpret_cast<uint4*>(smem + s * Cfg::STAGE + Cfg::OFF_K + Cfg::CHUNK)[i] = make_uint4(0, 0, 0, 0);
-                reinterpret_cast<uint4*>(smem + s * Cfg::STAGE + Cfg::OFF_LO + Cfg::CHUNK)[i] = make_uint4(0, 0, 0, 0);
-            }
-        fence_proxy_async_smem();
-    }
     if (warp == 1) {
-        tmem_alloc(misc, Cfg::TMEM_COLS);
+        tmem_alloc(misc + X_TMEM, Cfg::TMEM_COLS);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = misc[0];
+    const uint32_t tmem = misc[X_TMEM];
+
+    // this CTA's rows of the state slice it updates, read up front by the
+    // transform warps (idle until the first tile lands; their latency hides
+    // behind the token stream)
+    const int rows_per = (D + p.CL - 1) / p.CL;
+    const int r0 = min(D, rank * rows_per), r1 = min(D, r0 + rows_per);
+    constexpr int C4 = NV / 4;                          // float4 per row of the slice
+    constexpr int PRE = 4;                              // float4 items prefetched per transform thread
+    constexpr int NT = 32 * Cfg::TW;                    // transform threads
+    const int tt = tid - 64;                            // transform thread index (< 0 for warps 0, 1)
+    float* Sg = p.S + (size_t)bh * D * D + grp * NV;
+    float4 s_old[PRE];
+    if (tt >= 0) {
+#pragma unroll
+        for (int it = 0; it < PRE; ++it) {
+            const int e = tt + it * NT;
+            if (e < (r1 - r0) * C4)
+                s_old[it] = *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / C4) * D + 4 * (e % C4));
+        }
+    }
 
     if (warp == 0) {
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
             bool ok = true;
             int i = 0;
             for (; i < my_tiles && ok; ++i) {
-                const int s = i % Cfg::NS;
-                if (i >= Cfg::NS) ok = mbar_wait(&bar[A_EMPTY + s], ((i / Cfg::NS) & 1) ^ 1, wc, SITE_ABSORB_EMPTY);
+                const int s = i % NS;
+                if (i >= NS) ok = mbar_wait(&bar[Cfg::B_EMPTY + s], ((i / NS) - 1) & 1, wc, SITE_ABSORB_EMPTY);
                 if (!ok) break;
                 uint8_t* st = smem + s * Cfg::STAGE;
                 const int row = (t_begin + i) * Cfg::TT;
-                mbar_arrive_expect_tx(&bar[A_FULL + s], 2 * Cfg::TT * D * 2);
-                for (int m = 0; m < D / 64; ++m) {
-                    tma_load_3d(st + Cfg::OFF_K + m * Cfg::CHUNK, &tmK, &bar[A_FULL + s], 64 * m, row, bh);
-                    tma_load_3d(st + Cfg::OFF_V + m * Cfg::CHUNK, &tmV, &bar[A_FULL + s], 64 * m, row, bh);
-                }
+                mbar_arrive_expect_tx(&bar[Cfg::B_FULL + s], Cfg::STAGE);
+                for (int m = 0; m < D / 64; ++m)
+                    tma_load_3d(st + m * Cfg::CHUNK, &tmK, &bar[Cfg::B_FULL + s], 64 * m, row, bh);
+                for (int m = 0; m < NV / 64; ++m)
+                    tma_load_3d(st + Cfg::K_BYTES + m * Cfg::CHUNK, &tmV, &bar[Cfg::B_FULL + s], grp * NV + 64 * m,
+                                row, bh);
             }
-            if (!ok) {
-                for (int v = max(0, i - Cfg::NS); v < i; ++v) {
-                    const uint32_t a = smem_u32(&bar[A_FULL + v % Cfg::NS]);
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(a, (v / Cfg::NS) & 1) && globaltimer_ns() - t0 < p.wait_limit_ns) {
-                    }
+            // bounded drain: every load issued has landed before the CTA goes on
+            for (int v = (i > NS ? i - NS : 0); v < i; ++v) {
+                const uint32_t a = smem_u32(&bar[Cfg::B_FULL + v % NS]);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(a, (v / NS) & 1) && globaltimer_ns() - t0 < p.wait_limit_ns) {
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
         if (lane == 0) {
             bool ok = true;
             for (int i = 0; i < my_tiles && ok; ++i) {
-                const int s = i % Cfg::NS;
-                const int a = i & 1;
-                ok = mbar_wait(&bar[A_PHI + s], (i / Cfg::NS) & 1, wc, SITE_ABSORB_PHI);
-                if (ok && i >= 2) ok = mbar_wait(&bar[A_ACC_FREE + a], ((i >> 1) & 1) ^ 1, wc, SITE_ABSORB_ACC);
+                const int s = i % NS, as = i % NA, a = i & 1;
+                ok = mbar_wait(&bar[Cfg::B_PHI + as], (i / NA) & 1, wc, SITE_ABSORB_PHI);
+                if (ok && i >= 2) ok = mbar_wait(&bar[Cfg::B_ACC_FREE + a], ((i >> 1) - 1) & 1, wc, SITE_ABSORB_ACC);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * Cfg::STAGE);
+                const uint64_t vdesc = smem_desc(smem_u32(smem + s * Cfg::STAGE + Cfg::K_BYTES), Cfg::CHUNK, 1024);
+                const uint32_t acc = tmem + Cfg::ACC0 + a * NV;
+                const uint32_t at = tmem + as * Cfg::A_COLS;
 #pragma unroll
                 for (int hl = 0; hl < 2; ++hl) {
-                    const uint32_t a0 = st + (hl ? Cfg::OFF_LO : Cfg::OFF_K);
 #pragma unroll
-                    for (int kk = 0; kk < Cfg::TT / 16; ++kk) {
-                        mma_ss(tmem + a * 128, smem_desc(a0 + kk * 2048, Cfg::CHUNK, 1024),
-                               smem_desc(st + Cfg::OFF_V + kk * 2048, Cfg::CHUNK, 1024), Cfg::IDESC,
+                    for (int kk = 0; kk < Cfg::TT / 16; ++kk)
+                        mma_ts(acc, at + 32 * hl + 8 * kk, vdesc + (uint64_t)((kk * 2048) >> 4), Cfg::IDESC,
                                (hl > 0 || kk > 0) ? 1u : 0u);
-                    }
                 }
-                mma_commit(&bar[A_EMPTY + s]);
-                mma_commit(&bar[A_ACC_FULL + a]);
+                mma_commit(&bar[Cfg::B_EMPTY + s]);
+                mma_commit(&bar[Cfg::B_ACC_FULL + a]);
             }
-            mma_commit(&bar[A_DRAIN]);
-            const uint32_t a = smem_u32(&bar[A_DRAIN]);
+            // drain (bounded): every MMA issued has completed
+            mma_commit(&bar[Cfg::B_DRAIN]);
+            const uint32_t a = smem_u32(&bar[Cfg::B_DRAIN]);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(a, 0)) {
                 if (globaltimer_ns() - t0 > p.wait_limit_ns) {
@@ -186,119 +232,112 @@ __global__ void __launch_bounds__(320, 1)
         }
         __syncwarp();
     } else {
-        // ---- phi transform: thread -> column pair cp, row group rg ----------
-        const int t = tid - 64;                 // 0..255
-        constexpr int NCP = D / 2;              // column pairs
-        constexpr int NRG = 256 / NCP;          // row groups (4 for d=128, 8 for d=64)
-        const int cp = t % NCP, rg = t / NCP;
-        const int col = 2 * cp;
-        const uint32_t coff = (uint32_t)(col / 64) * Cfg::CHUNK;
-        // accumulator drain: warp -> TMEM lane quarter, column half
-        constexpr int DC = D / 2;               // columns per draining thread
-        const int quarter = warp & 3;
-        const int chalf = (warp - 2) >> 2;
-        const int row = quarter * 32 + lane;
-        float racc[DC];
+        // ---------------- phi transform + accumulator folding ----------------
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int tq = (warp - 2) >> 2;          // token quarter of a tile, column quarter of the accumulator
+        const int f = 32 * q + lane;             // feature (TMEM lane)
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        constexpr int NC = Cfg::NC;
+        const uint8_t* kcol0 = smem + (uint32_t)(f / 64) * Cfg::CHUNK;
+        float racc[NC];
 #pragma unroll
-        for (int k = 0; k < DC; ++k) racc[k] = 0.0f;
-        float z0 = 0.0f, z1 = 0.0f;
+        for (int k = 0; k < NC; ++k) racc[k] = 0.0f;
+        float z_run = 0.0f;
         bool ok = true;
-        auto drain = [&](int j) -> bool {
+        auto fold = [&](int j) -> bool {
             const int a = j & 1;
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[A_ACC_FULL + a], (j >> 1) & 1, wc, SITE_ABSORB_ACC)))
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[Cfg::B_ACC_FULL + a], (j >> 1) & 1, wc, SITE_ABSORB_ACC)))
                 return false;
             tc_fence_after();
 #pragma unroll
-            for (int c0 = 0; c0 < DC; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + a * 128 + chalf * DC + c0, v);
+            for (int c0 = 0; c0 < NC; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16_nw(tmem + lane_base + Cfg::ACC0 + a * NV + tq * NC + c0, v);
+                tmem_wait_ld();
+                reg_dep16(v);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) racc[c0 + k] = __fadd_rn(racc[c0 + k], __uint_as_float(v[k]));
+                for (int k = 0; k < 16; ++k) racc[c0 + k] = __fadd_rn(racc[c0 + k], __uint_as_float(v[k]));
             }
             tc_fence_before();
-            mbar_arrive(&bar[A_ACC_FREE + a]);
+            mbar_arrive(&bar[Cfg::B_ACC_FREE + a]);
             return true;
         };
+        constexpr float kLog2e = 1.4426950408889634f;
         for (int i = 0; i < my_tiles && ok; ++i) {
-            const int s = i % Cfg::NS;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[A_FULL + s], (i / Cfg::NS) & 1, wc, SITE_ABSORB_FULL));
+            const int s = i % NS, as = i % NA;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[Cfg::B_FULL + s], (i / NS) & 1, wc, SITE_ABSORB_FULL));
             if (!ok) break;
-            uint8_t* st = smem + s * Cfg::STAGE;
-            const int tok0 = (t_begin + i) * Cfg::TT;
-            // all rows are loaded before any is written back (the in-place stores
-            // could otherwise alias the next row's load, serializing the rows);
-            // rows past the last token (a partial tile) become phi = 0
-            constexpr int RPT = Cfg::TT / NRG;   // rows per thread
-            uint32_t kv[RPT];
+            const uint8_t* kt = kcol0 + s * Cfg::STAGE;
+            const int tok0 = (t_begin + i) * Cfg::TT + Cfg::TPW * tq;   // first token of this warp's quarter tile
+            const bool full = (t_begin + i + 1) * Cfg::TT <= p.n;
+            // the quarter tile's keys of feature f (bf16 -> fp32 is a shift)
+            float xk[Cfg::TPW];
 #pragma unroll
-            for (int k = 0; k < RPT; ++k)
-                kv[k] = *reinterpret_cast<const uint32_t*>(st + Cfg::OFF_K + coff + sw128_offset(rg + k * NRG, col % 64));
-#pragma unroll
-            for (int k = 0; k < RPT; ++k) {
-                const int r = rg + k * NRG;
-                const bool valid = tok0 + r < p.n;
-                float a = bf16_lo(kv[k]), b = bf16_hi(kv[k]);
-                a = a > 0.0f ? a + 1.0f : __expf(a);
-                b = b > 0.0f ? b + 1.0f : __expf(b);
-                a = valid ? a : 0.0f;
-                b = valid ? b : 0.0f;
-                z0 += a;
-                z1 += b;
-                const uint32_t hi = pack_bf16(a, b);
-                const uint32_t off = coff + sw128_offset(r, col % 64);
-                *reinterpret_cast<uint32_t*>(st + Cfg::OFF_K + off) = hi;
-                *reinterpret_cast<uint32_t*>(st + Cfg::OFF_LO + off) = pack_bf16(a - bf16_lo(hi), b - bf16_hi(hi));
+            for (int t = 0; t < Cfg::TPW; ++t) {
+                uint32_t h16 = 0;
+                if (f < D)
+                    h16 = *reinterpret_cast<const uint16_t*>(kt + sw128_offset(Cfg::TPW * tq + t, (uint32_t)(f % 64)));
+                xk[t] = __uint_as_float(h16 << 16);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bar[A_PHI + s]);
-            if (i >= 1) ok = drain(i - 1);
+            // phi(x) = max(x, 0) + exp(min(x, 0)) (= elu(x) + 1), two tokens per
+            // step; hi = rn(phi), lo = rn(phi - hi)
+            uint32_t hi[Cfg::TPW / 2], lo[Cfg::TPW / 2];
+            float za = 0.0f, zb = 0.0f;   // this quarter tile's even / odd tokens: short chains
+#pragma unroll
+            for (int j = 0; j < Cfg::TPW / 2; ++j) {
+                const float xa = xk[2 * j], xb = xk[2 * j + 1];
+                float ea, eb;
+                mul2(ea, eb, fminf(xa, 0.0f), fminf(xb, 0.0f), kLog2e, kLog2e);
+                ea = ex2_approx(ea);
+                eb = ex2_approx(eb);
+                float ya, yb;
+                add2(ya, yb, fmaxf(xa, 0.0f), fmaxf(xb, 0.0f), ea, eb);
+                if (!full) {   // tokens past the last evicted one (and features past d) carry phi = 0
+                    ya = (f < D && tok0 + 2 * j < p.n) ? ya : 0.0f;
+                    yb = (f < D && tok0 + 2 * j + 1 < p.n) ? yb : 0.0f;
+                } else if (f >= D) {
+                    ya = yb = 0.0f;
+                }
+                add2(za, zb, za, zb, ya, yb);
+                const uint32_t h = pack_bf16(ya, yb);
+                hi[j] = h;
+                float ra, rb;   // phi - hi, with -hi taken from the packed bits (sign flipped)
+                add2(ra, rb, ya, yb, __uint_as_float((h << 16) ^ 0x80000000u),
+                     __uint_as_float((h & 0xFFFF0000u) ^ 0x80000000u));
+                lo[j] = pack_bf16(ra, rb);
+            }
+            z_run += za + zb;
+            const uint32_t at = tmem + lane_base + as * Cfg::A_COLS + (Cfg::TPW / 2) * tq;
+            tmem_st8_nw(at, hi);
+            tmem_st8_nw(at + 32, lo);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bar[Cfg::B_PHI + as]);
+            if (i >= 1) ok = fold(i - 1);
         }
-        if (ok && my_tiles > 0) ok = drain(my_tiles - 1);
-        zp[rg * D + col] = z0;
-        zp[rg * D + col + 1] = z1;
-        // ---- partial state -> shared memory (over stage 0) ----------------
-        __syncwarp();
-        float* part = reinterpret_cast<float*>(smem);   // [128][PITCH], over the stage buffers
-        // every load was consumed above, and the last MMA has been drained.
+        if (ok && my_tiles > 0) ok = fold(my_tiles - 1);
+        // every load was consumed and the last MMA has completed (its
+        // accumulator was folded), so the stage buffers are free: partial
+        // state [128][PITCH] over them
+        float* part = reinterpret_cast<float*>(smem);
         if (ok) {
 #pragma unroll
-            for (int k = 0; k < DC; k += 4)
-                *reinterpret_cast<float4*>(part + row * Cfg::PITCH + chalf * DC + k) =
+            for (int k = 0; k < NC; k += 4)
+                *reinterpret_cast<float4*>(part + f * Cfg::PITCH + tq * NC + k) =
                     make_float4(racc[k], racc[k + 1], racc[k + 2], racc[k + 3]);
+            zp[tq * 128 + f] = z_run;
         } else {
             *wc.abort_flag = 1;
         }
     }
-    // this rank's rows of S, read while the other CTAs of the cluster finish
-    const int rows_per = (D + p.CL - 1) / p.CL;
-    const int r0 = rank * rows_per, r1 = min(D, r0 + rows_per);
-    float* Sg = p.S + (size_t)bh * D * D;
-    constexpr int ITEMS = (D / 8) * (D / 4) / Cfg::NTHR + 1;   // float4 items per thread (rows_per <= D/8 for CL = 8)
-    float4 s_old[ITEMS];
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int e = tid + it * Cfg::NTHR;
-        if (e < (r1 - r0) * (D / 4))
-            s_old[it] = *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / (D / 4)) * D + 4 * (e % (D / 4)));
-    }
     tc_fence_before();
     __syncthreads();
-    // z partial of this CTA: fixed order over row groups
-    if (tid < D) {
-        constexpr int NRG = 256 / (D / 2);
-        float acc = 0.0f;
-        for (int g2 = 0; g2 < NRG; ++g2) acc += zp[g2 * D + tid];
-        zp[7 * D + tid] = acc;   // slot 7 (>= NRG for d=128; for d=64 read after the sum)
-    }
     cluster.sync();
-    // ---- cluster reduction: rank r owns rows [r0, r1) of S ----------------
+    // ---- cluster reduction: rank r owns rows [r0, r1) of this group's columns ----
+    // (a CTA that gave up has recorded the error; the state is then undefined)
     if (*wc.abort_flag == 0) {
-        // all ranks' float4s of an item are requested first, then added in rank order;
-        // the first ITEMS items of a thread use the prefetched S, any further ones
-        // (clusters smaller than 8) read S here
-        const int total = (r1 - r0) * (D / 4);
-        auto reduce_item = [&](int e, float4 o) {
-            const int c = r0 + e / (D / 4), j = 4 * (e % (D / 4));
+        auto reduce_item = [&](int e, float4 old) {
+            const int c = r0 + e / C4, j = 4 * (e % C4);
             float4 v[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -315,23 +354,36 @@ __global__ void __launch_bounds__(320, 1)
                     acc.w += v[q].w;
                 }
             }
-            o.x += acc.x;
-            o.y += acc.y;
-            o.z += acc.z;
-            o.w += acc.w;
-            *reinterpret_cast<float4*>(Sg + (size_t)c * D + j) = o;
+            *reinterpret_cast<float4*>(Sg + (size_t)c * D + j) =
+                make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
         };
+        const int total = (r1 - r0) * C4;
+        if (tt >= 0) {
 #pragma unroll
-        for (int it = 0; it < ITEMS; ++it) {
-            const int e = tid + it * Cfg::NTHR;
-            if (e < total) reduce_item(e, s_old[it]);
-        }
-        for (int e = tid + ITEMS * Cfg::NTHR; e < total; e += Cfg::NTHR)
-            reduce_item(e, *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / (D / 4)) * D + 4 * (e % (D / 4))));
-        if (rank == 0 && tid < D) {
-            float acc = 0.0f;
-            for (int q = 0; q < p.CL; ++q) acc += cluster.map_shared_rank(zp, q)[7 * D + tid];
-            p.z[(size_t)bh * D + tid] += acc;
+            for (int it = 0; it < PRE; ++it) {
+                const int e = tt + it * NT;
+                if (e < total) reduce_item(e, s_old[it]);
+            }
+            for (int e = tt + PRE * NT; e < total; e += NT)
+                reduce_item(e, *reinterpret_cast<const float4*>(Sg + (size_t)(r0 + e / C4) * D + 4 * (e % C4)));
+        } else if (grp == 0 && rank == 0) {
+            // z: warps 0 and 1, one feature per thread (rows d..127 of the
+            // d = 64 case are zero); every rank's four partials requested first
+            for (int c = tid; c < D; c += 64) {
+                float4 zv[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (q < p.CL) {
+                        const float* zq = cluster.map_shared_rank(zp, q);
+                        zv[q] = make_float4(zq[c], zq[128 + c], zq[256 + c], zq[384 + c]);
+                    }
+                }
+                float acc = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < p.CL) acc += (zv[q].x + zv[q].y) + (zv[q].z + zv[q].w);
+                p.z[(size_t)bh * D + c] += acc;
+            }
         }
     }
     cluster.sync();
@@ -341,28 +393,82 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-template <int D>
-int launch_absorb_t(const CUtensorMap& tk, const CUtensorMap& tv, const AbsParams& p, cudaStream_t st)
+template <int D, int NV>
+cudaLaunchConfig_t absorb_launch_cfg(int grid, int CL, cudaStream_t st, cudaLaunchAttribute* attr)
 {
-    using Cfg = AbsCfg<D>;
-    auto kern = absorb_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
-    if (e != cudaSuccess) return (int)e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.BH * p.CL);
-    cfg.blockDim = dim3(Cfg::NTHR);
-    cfg.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(AbsCfg<D, NV>::NTHR);
+    cfg.dynamicSmemBytes = AbsCfg<D, NV>::SMEM_ALLOC;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = p.CL;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cfg;
+}
+
+// Clusters of CL CTAs of absorb_kernel<D, NV> that fit on the device at
+// once (cached per device; 0 if the query fails).
+template <int D, int NV>
+int max_clusters(int dev, int CL)
+{
+    static std::mutex mu;
+    static int cache[64][9] = {};
+    if (dev < 0 || dev >= 64 || CL < 1 || CL > 8) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev][CL] == 0) {
+        auto kern = absorb_kernel<D, NV>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AbsCfg<D, NV>::SMEM_ALLOC) !=
+            cudaSuccess)
+            return 0;
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV>(CL, CL, 0, attr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            return 0;
+        }
+        cache[dev][CL] = n;
+    }
+    return cache[dev][CL];
+}
+
+template <int D, int NV>
+int launch_absorb_t(const CUtensorMap& tk, const CUtensorMap& tv, AbsParams p, cudaStream_t st)
+{
+    using Cfg = AbsCfg<D, NV>;
+    auto kern = absorb_kernel<D, NV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
+    if (e != cudaSuccess) return (int)e;
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV>(p.BH * p.NG * p.CL, p.CL, st, attr);
     e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
+}
+
+// The launch shape: NG column groups per head and CL CTAs per cluster, the
+// most CTAs (counted up to one per SM) whose clusters are all resident at
+// once; on ties, the larger cluster, and fewer column groups (fewer repeated
+// key reads).  Clusters of one CTA never wait on each other, so they may run
+// in several waves.
+template <int D, int NV>
+void pick_shape(int BH, int n_tiles, int sms, int dev, int NG, int& best_cl, int& best_score)
+{
+    for (int CL = 8; CL >= 1; --CL) {
+        if (CL > n_tiles && CL > 1) continue;
+        const long clusters = (long)BH * NG;
+        const long ctas = clusters * CL;
+        if (CL > 1 && (ctas > sms || clusters > max_clusters<D, NV>(dev, CL))) continue;
+        const int score = (int)(ctas < sms ? ctas : sms);
+        if (score > best_score) {
+            best_score = score;
+            best_cl = CL;
+        }
+    }
 }
 
 }  // namespace
@@ -372,20 +478,35 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
 {
     alignas(64) CUtensorMap tk, tv;
     const uint64_t hs = (uint64_t)head_stride * g.d * 2;
-    int e = make_tmap_bf16_3d(&tk, K_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, AbsCfg<128>::TT);
+    constexpr int TT = AbsCfg<128, 64>::TT;
+    int e = make_tmap_bf16_3d(&tk, K_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, TT);
     if (e) return e;
-    e = make_tmap_bf16_3d(&tv, V_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, AbsCfg<128>::TT);
+    e = make_tmap_bf16_3d(&tv, V_ev, g.d, (uint64_t)n_ev, g.BH, (uint64_t)g.d * 2, hs, 64, TT);
     if (e) return e;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int n_tiles = (n_ev + AbsCfg<128>::TT - 1) / AbsCfg<128>::TT;
-    int CL = sms / (g.BH > 0 ? g.BH : 1);
-    CL = CL < 1 ? 1 : (CL > 8 ? 8 : CL);
-    CL = CL > n_tiles ? n_tiles : CL;
-    AbsParams p{g.BH, n_ev, CL, S, z, status, wait_limit_ns};
+    const int n_tiles = (n_ev + TT - 1) / TT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return g.d == 128 ? launch_absorb_t<128>(tk, tv, p, st) : launch_absorb_t<64>(tk, tv, p, st);
+    AbsParams p{g.BH, n_ev, 1, 1, S, z, status, wait_limit_ns};
+    if (g.d == 64) {
+        int cl = 1, ctas = 0;
+        pick_shape<64, 64>(g.BH, n_tiles, sms, dev, 1, cl, ctas);
+        p.CL = cl;
+        return launch_absorb_t<64, 64>(tk, tv, p, st);
+    }
+    int cl1 = 1, c1 = 0, cl2 = 1, c2 = 0;
+    pick_shape<128, 128>(g.BH, n_tiles, sms, dev, 1, cl1, c1);
+    pick_shape<128, 64>(g.BH, n_tiles, sms, dev, 2, cl2, c2);
+    // two column groups compute phi of every key twice: worth it only for
+    // clearly more CTAs
+    if (2 * c2 > 3 * c1) {
+        p.NG = 2;
+        p.CL = cl2;
+        return launch_absorb_t<128, 64>(tk, tv, p, st);
+    }
+    p.CL = cl1;
+    return launch_absorb_t<128, 128>(tk, tv, p, st);
 }
 
 }  // namespace hf

@@ -293,7 +293,7 @@ hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_
     float* qp = reinterpret_cast<float*>(w + L.qp);
     float* kp = reinterpret_cast<float*>(w + L.kp);
     HF_LAUNCH(launch_pool(Q, Kc, g, window_frames(sm, n_win), qp, kp, stream), "pool launch");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, scores, nullptr, nullptr, nullptr, stream), "score launch");
+    HF_LAUNCH(launch_scores(qp, kp, g, sm, scores, stream), "score launch");
     return HF_OK;
 }
 
@@ -377,7 +377,6 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
     const Geom g = make_geom(cfg, n_win, slot_stride);
     const WsLayout L = ws_layout(cfg);
     uint8_t* w = static_cast<uint8_t*>(ws);
-    float* qp = reinterpret_cast<float*>(w + L.qp);
     float* kp = reinterpret_cast<float*>(w + L.kp);
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + L.idx);
     uint16_t* smma = reinterpret_cast<uint16_t*>(w + L.smma);
@@ -398,18 +397,18 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
                    : (int)cudaEventRecord(e, st);
     };
     PoolFrames pf = window_frames(sm, n_win);
+    pf.with_q = 0;
     if (flags & HF_FWD_CACHED_KEYS) pf.n = 0;   // the window's key blocks are already in the cache
     HF_LAUNCH(mark(0), "event record");
-    HF_LAUNCH(launch_pool(Q, Kc, g, pf, qp, kp, stream), "pool launch");
+    HF_LAUNCH(launch_pool_keys(Kc, g, pf, kp, status, kDefaultWaitLimitNs, stream), "key pooling launch");
     HF_LAUNCH(mark(1), "event record");
-    HF_LAUNCH(launch_score_select(qp, kp, g, sm, nullptr, idx, prounds, counters, stream), "score/select launch");
+    HF_LAUNCH(launch_fwd_prologue(Q, kp, S, g, sm, idx, smma, prounds, counters, status, kDefaultWaitLimitNs, stream),
+              "prologue launch");
     HF_LAUNCH(mark(2), "event record");
-    HF_LAUNCH(launch_smma_prep(S, g, smma, stream), "state prep launch");
-    HF_LAUNCH(mark(3), "event record");
     HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, smma, z, nullptr, O, prounds, partial, counters, status,
                           kDefaultWaitLimitNs, stream),
               "hybrid attention launch");
-    HF_LAUNCH(mark(4), "event record");
+    HF_LAUNCH(mark(3), "event record");
     return HF_OK;
 }
 
@@ -560,7 +559,8 @@ hf_status hf_pool_keys(const hf_config* cfg, const uint16_t* Kc, int32_t slot_st
     const Geom g = make_geom(cfg, cfg->chunk_frames, slot_stride);
     const WsLayout L = ws_layout(cfg);
     float* kp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.kp);
-    HF_LAUNCH(launch_pool(nullptr, Kc, g, pf, nullptr, kp, stream), "key pool launch");
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + L.status);
+    HF_LAUNCH(launch_pool_keys(Kc, g, pf, kp, status, kDefaultWaitLimitNs, stream), "key pool launch");
     return HF_OK;
 }
 

@@ -32,6 +32,8 @@ enum Site : uint32_t {
     SITE_ABSORB_ACC = 204,
     SITE_ABSORB_DRAIN = 205,
     SITE_SELFTEST = 301,
+    SITE_PROLOGUE_Q = 401,
+    SITE_POOL_KEYS = 402,
 };
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;   // 2 s
@@ -70,8 +72,8 @@ struct Geom {
 struct WsLayout {
     size_t status;   // 256 B: uint32 [0] code, [1] site
     size_t counters; // uint32 [BH * pairs per head][2]: parts of a split pair that arrived (zero between calls)
-    size_t qp;       // fp32 [BH][nQB][d]
-    size_t kp;       // fp32 [BH][W slots][d][bpf]: pooled keys of every ring slot (kept between calls)
+    size_t qp;       // fp32 [BH][nQB][d] (hf_block_scores)
+    size_t kp;       // fp32 [BH][W slots][d/4][bpf][4]: pooled keys of every ring slot (kept between calls)
     size_t idx;      // int32 [BH][nQB][K_max]
     size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout)
     size_t prounds;  // int32 [BH * pairs per head]: rounds of each tile pair's slab stream
@@ -87,16 +89,24 @@ constexpr int kAttnMaxGrid = 160;
 // ---- launchers (return cudaError_t as int) --------------------------------
 int launch_pool(const uint16_t* Q, const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* qp, float* kpc,
                 void* stream);
-// pair_rounds (optional): rounds of each tile pair's slab stream for the attention
-// kernel's balancing; with it, counters (the pairs' arrival counters) are zeroed.
-int launch_score_select(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores,
-                        int32_t* idx, int32_t* pair_rounds, uint32_t* counters, void* stream);
+// Scores of pooled query blocks qp [BH][nQB][d] against the window's cached
+// key pools (the standalone hf_block_scores).
+int launch_scores(const float* qp, const float* kpc, const Geom& g, const SlotMap& sm, float* scores, void* stream);
 int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
+// The hybrid forward's prologue in one launch: pooling of the chunk's query
+// blocks, the state as the epilogue's tensor-core operand (S -> bf16 hi/lo),
+// scores against the cached key pools, top-K and, when pair_rounds is given,
+// each tile pair's round count (and its arrival counters zeroed).
+int launch_fwd_prologue(const uint16_t* Q, const float* kpc, const float* S, const Geom& g, const SlotMap& sm,
+                        int32_t* idx, uint16_t* smma, int32_t* pair_rounds, uint32_t* counters, uint32_t* status,
+                        uint64_t wait_limit_ns, void* stream);
+// Key-block pooling of ring slots pf.slot[0..pf.n) into the cache, bulk copies.
+int launch_pool_keys(const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* kpc, uint32_t* status,
+                     uint64_t wait_limit_ns, void* stream);
 int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const Geom& g, const SlotMap& sm,
                 const int32_t* idx, const uint16_t* smma, const float* z, float* o_swa, uint16_t* o_bf16,
                 const int32_t* pair_rounds, float* partial, uint32_t* counters, uint32_t* status,
                 uint64_t wait_limit_ns, void* stream);
-int launch_smma_prep(const float* S, const Geom& g, uint16_t* smma, void* stream);
 
 // Relative temporal RoPE pre-step: element (h, f, t, c) at
 // h * head_stride + slot[f] * frame_stride + t * d + c (src and dst alike).

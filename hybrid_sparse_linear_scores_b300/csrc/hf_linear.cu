@@ -1,7 +1,8 @@
 // hf_linear.cu -- the linear temporal attention read outside the fused
 // forward (Hybrid Forcing, English technical summary, section 2.A.1 "Linear
-// Temporal Attention"), the state reset, the preparation of the state as a
-// tensor-core operand, and the bounded-wait self-test kernel.
+// Temporal Attention"), the state reset, and the bounded-wait self-test
+// kernel.  (The fused forward's state operand is prepared by the prologue
+// kernel in hf_select.cu.)
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -11,35 +12,6 @@
 
 namespace hf {
 namespace {
-
-// S fp32 [BH][d][d] -> bf16 hi = rn(S), lo = rn(S - hi), laid out as the
-// B operand of the fused linear-read MMA: MN-major (value channel j
-// contiguous), 128-byte swizzle, per head [hi|lo][j/64][row c][128 B].
-__global__ void smma_prep_kernel(const float* __restrict__ S, Geom g, uint16_t* __restrict__ smma)
-{
-    const int d = g.d;
-    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;   // one thread per 8 consecutive j
-    const long per_head = (long)d * d / 8;
-    if (i >= (long)g.BH * per_head) return;
-    const int bh = (int)(i / per_head);
-    const int rem = (int)(i - (long)bh * per_head);
-    const int c = rem / (d / 8);
-    const int j0 = (rem - c * (d / 8)) * 8;
-    const float4* src = reinterpret_cast<const float4*>(S + ((size_t)bh * d + c) * d + j0);
-    const float4 a = src[0], b = src[1];
-    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        hi[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
-        lo[k] = pack_bf16(x[2 * k] - bf16_lo(hi[k]), x[2 * k + 1] - bf16_hi(hi[k]));
-    }
-    uint8_t* base = reinterpret_cast<uint8_t*>(smma) + (size_t)bh * 2 * d * d * 2;
-    const uint32_t off = (uint32_t)(j0 / 64) * (uint32_t)(d * 128) + c * 128u +
-                         ((((uint32_t)(j0 % 64) >> 3) ^ ((uint32_t)c & 7u)) << 4);
-    *reinterpret_cast<uint4*>(base + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(base + (size_t)d * d * 2 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-}
 
 // Standalone linear read in fp32 on CUDA cores: o = phi(q)^T S / (phi(q)^T z + eps).
 // CTA = 256 threads handles ROWS query rows of one head; S and z of the head
@@ -123,13 +95,6 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns)
 }
 
 }  // namespace
-
-int launch_smma_prep(const float* S, const Geom& g, uint16_t* smma, void* stream)
-{
-    const long n = (long)g.BH * g.d * g.d / 8;
-    smma_prep_kernel<<<(unsigned)((n + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(S, g, smma);
-    return (int)cudaGetLastError();
-}
 
 template <int D>
 static int launch_lr(const uint16_t* Q, const float* S, const float* z, const Geom& g, float* O, int accumulate,

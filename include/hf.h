@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HF_ABI_VERSION 1
+#define HF_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define HF_API __attribute__((visibility("default")))
@@ -188,7 +188,7 @@ HF_API hf_status hf_hybrid_forward(const hf_config *cfg, const uint16_t *Q, cons
 
 /* Key-block pooling for the pooled-key cache (English technical summary,
  * section 2.A.2: the block importance scores use pooled key blocks).  The
- * workspace keeps the pooled keys of every ring slot, fp32 [b, H, W, d, bpf]
+ * workspace keeps the pooled keys of every ring slot, fp32 [b, H, W, d/4, bpf, 4]
  * (W = cfg->window_frames slots), between calls; a frame's key blocks do not
  * change while it stays in the window, so they need to be pooled only once,
  * when the frame is written into its slot.  This call pools the key blocks
@@ -242,6 +242,9 @@ HF_API hf_status hf_rope_relative(const hf_config *cfg, const uint16_t *src, uin
                                   or by an earlier forward, since it was last written);
                                   only the chunk's queries are pooled */
 
+/* Number of timing points of hf_hybrid_forward_ex / _profiled. */
+#define HF_FWD_EVENTS 4
+
 /* hf_hybrid_forward with options: `flags` (HF_FWD_CACHED_KEYS or 0) and
  * per-kernel timing, `events` as in hf_hybrid_forward_profiled (may be NULL).
  * Without HF_FWD_CACHED_KEYS every call pools the keys of the whole window
@@ -251,21 +254,25 @@ HF_API hf_status hf_hybrid_forward_ex(const hf_config *cfg, const uint16_t *Q, c
                                       const int32_t *slot_map /* host */, int32_t n_win,
                                       const float *S, const float *z, uint16_t *O, int32_t *idx_out,
                                       void *ws, void *stream, uint32_t flags,
-                                      void *const *events /* host, 5 entries, or NULL */);
+                                      void *const *events /* host, HF_FWD_EVENTS entries, or NULL */);
 
-/* hf_hybrid_forward with per-kernel timing: events[0..4] (cudaEvent_t
- * handles created by the caller, or NULL for none) are recorded on `stream`
- * before the pooling kernel, before the score/select kernel, before the state
- * preparation kernel, before the attention kernel and after it.  The results
- * are identical to hf_hybrid_forward.  When `stream` is being captured into
- * a CUDA graph the events are captured as external event records, so they
- * time every replay of the graph. */
+/* hf_hybrid_forward with per-kernel timing.  The forward runs at most three
+ * kernels: the window's key pooling (skipped with HF_FWD_CACHED_KEYS), the
+ * prologue (query pooling, the state as the epilogue's tensor-core operand,
+ * scores, top-K, the attention kernel's work split) and the attention kernel
+ * (sparse softmax attention with the linear read and the sum fused in).
+ * events[0..3] (cudaEvent_t handles created by the caller, or NULL for none)
+ * are recorded on `stream` before the key pooling, before the prologue,
+ * before the attention kernel and after it.  The results are identical to
+ * hf_hybrid_forward.  When `stream` is being captured into a CUDA graph the
+ * events are captured as external event records, so they time every replay
+ * of the graph. */
 HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
                                             const uint16_t *Vc, int32_t slot_stride,
                                             const int32_t *slot_map /* host */, int32_t n_win,
                                             const float *S, const float *z, uint16_t *O,
                                             int32_t *idx_out, void *ws, void *stream,
-                                            void *const *events /* host, 5 entries */);
+                                            void *const *events /* host, HF_FWD_EVENTS entries */);
 
 /* Size of the static device scratch that hf_hybrid_forward_noalloc uses in
  * place of a workspace: 16 MiB, enough for the workspace (without its
