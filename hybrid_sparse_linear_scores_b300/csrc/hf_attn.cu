@@ -152,7 +152,8 @@ struct AttnCfg {
     static constexpr int OFF_BAR = OFF_CODE + MAX_SLABS / 2 + 16;
     static constexpr int NBAR = 32;
     static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;               // uint32[32]
-    static constexpr int SMEM = OFF_MISC + 128;
+    static constexpr int OFF_Z = OFF_MISC + 128;                      // fp32 [D]: z of the pair's head
+    static constexpr int SMEM = OFF_Z + D * 4;
     static constexpr int SMEM_ALLOC = SMEM + 1024;                    // slack for 1 KB alignment
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC_QK64 = idesc_bf16_f32(128, 64, false, false);
@@ -439,7 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the Q tiles depend only on the pair, so they load while the list is built
                 // (the previous pair's output store has finished reading the Q region)
                 const int ntiles = (nblk[0] > 0) + (nblk[1] > 0);
-                mbar_arrive_expect_tx(&bar[B_Q], ntiles * Cfg::G * Cfg::DCH * BETA * 128);
+                // (with the fused epilogue, z of the head rides along: the
+                // linear read's denominators then read it from shared memory)
+                mbar_arrive_expect_tx(&bar[B_Q], ntiles * Cfg::G * Cfg::DCH * BETA * 128 + (FUSED ? D * 4 : 0));
+                if (FUSED) bulk_load(smem + Cfg::OFF_Z, p.z + (size_t)bh * D, D * 4, &bar[B_Q]);
                 for (int t = 0; t < 2; ++t) {
                     if (nblk[t] == 0) continue;
                     uint8_t* sQ = smem + Cfg::OFF_Q + t * Cfg::Q_BYTES;
@@ -1056,38 +1060,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // (a tile that took part in no round of this part waits for its Q tile
                         // here; otherwise its S_FULL waits already covered the Q load)
                         tc_fence_after();
-                        // phi(q) (bf16, in place over Q) and the linear-read denominator.  The
-                        // row is loaded whole, transformed in registers (z read alongside, four
-                        // independent denominator chains) and stored whole: a store between
-                        // the loads would order every later load behind it.
-                        const float4* zh = reinterpret_cast<const float4*>(p.z + (size_t)bh * D);
-                        uint4 qv[Cfg::DCH * 8];   // 16-byte chunk k = channels [8k, 8k + 8)
-#pragma unroll
-                        for (int k = 0; k < Cfg::DCH * 8; ++k)
-                            qv[k] = *reinterpret_cast<const uint4*>(sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 +
-                                                                    ((((k & 7) ^ (r & 7)) & 7) << 4));
+                        // phi(q) (bf16, in place over Q) and the linear-read denominator (z
+                        // of the head from shared memory, four independent denominator
+                        // chains), two 16-byte chunks of the row per step.  This code runs
+                        // once per pair: kept as a small loop rather than unrolled over the
+                        // row, it is fetched once instead of as a long straight run of
+                        // instructions that all the group's warps wait for.
+                        const float4* zh = reinterpret_cast<const float4*>(smem + Cfg::OFF_Z);
                         float dn[4] = {g.eps, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+                        for (int k0 = 0; k0 < Cfg::DCH * 8; k0 += 2) {
+                            uint4 qv[2];
+                            uint8_t* qp2[2];
 #pragma unroll
-                        for (int k = 0; k < Cfg::DCH * 8; ++k) {
-                            const float4 za = __ldg(zh + 2 * k), zb = __ldg(zh + 2 * k + 1);
-                            const float zc[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
-                            uint32_t w4[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                float a = bf16_lo(w4[i]), bq = bf16_hi(w4[i]);
-                                a = a > 0.0f ? a + 1.0f : __expf(a);
-                                bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
-                                w4[i] = pack_bf16(a, bq);
-                                dn[i] = fmaf(bf16_lo(w4[i]), zc[2 * i], dn[i]);
-                                dn[i] = fmaf(bf16_hi(w4[i]), zc[2 * i + 1], dn[i]);
+                            for (int u = 0; u < 2; ++u) {
+                                const int k = k0 + u;
+                                qp2[u] = sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 + ((((k & 7) ^ (r & 7)) & 7) << 4);
+                                qv[u] = *reinterpret_cast<const uint4*>(qp2[u]);
                             }
-                            qv[k] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int k = k0 + u;
+                                const float4 za = zh[2 * k], zb = zh[2 * k + 1];
+                                const float zc[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
+                                uint32_t w4[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    float a = bf16_lo(w4[i]), bq = bf16_hi(w4[i]);
+                                    a = a > 0.0f ? a + 1.0f : __expf(a);
+                                    bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
+                                    w4[i] = pack_bf16(a, bq);
+                                    dn[i] = fmaf(bf16_lo(w4[i]), zc[2 * i], dn[i]);
+                                    dn[i] = fmaf(bf16_hi(w4[i]), zc[2 * i + 1], dn[i]);
+                                }
+                                *reinterpret_cast<uint4*>(qp2[u]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
                         }
                         const float den = (dn[0] + dn[1]) + (dn[2] + dn[3]);
-#pragma unroll
-                        for (int k = 0; k < Cfg::DCH * 8; ++k)
-                            *reinterpret_cast<uint4*>(sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 +
-                                                      ((((k & 7) ^ (r & 7)) & 7) << 4)) = qv[k];
                         fence_proxy_async_smem();
                         tc_fence_before();
                         mbar_arrive(&bar[B_PHIQ + t]);
