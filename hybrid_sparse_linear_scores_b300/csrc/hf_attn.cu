@@ -964,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float m_own = participated ? m_use : -INFINITY;
                         const float l_own = participated ? l_tot : 0.0f;
                         if (participated) tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                         for (int cb = 0; cb < D; cb += 64) {
                             uint32_t o[2][32];
                             if (participated) {
@@ -998,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             auto scale_of = [&](float mk) { return mk == -INFINITY ? 0.0f : ex2_approx((mk - m_all) * sl2); };
                             const float sc_own = scale_of(m_own);
                             float lt = 0.0f;
-#pragma unroll
+#pragma unroll 1
                             for (int cb = 0; cb < D; cb += 64) {
                                 float acc[64];
 #pragma unroll
@@ -1104,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok) {
                             tc_fence_after();
                             const float inv_den = 1.0f / den;
-#pragma unroll
+#pragma unroll 1
                             for (int cb = 0; cb < D; cb += 64) {
                                 uint32_t o[2][32], li[2][32];
                                 tmem_ld32_nw(o_col + cb, o[0]);
