@@ -434,6 +434,30 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
                                   "2 launches in one CUDA graph, L2 flushed before each replay"}
     del Qr, Kr
 
+    # the whole step with the relative RoPE on (EN section 2.C): absorb, rotation
+    # of the window's keys (ring -> rotated copy) and of the chunk's queries by
+    # their window-relative offsets, pooling of the rotated window's key blocks
+    # (every frame's offset moves with the window), prologue, attention
+    from hybrid_sparse_linear_scores_b300.stream import HybridAttentionLayer, RelativeRope
+    Lr = HybridAttentionLayer(cfg, dev, rope=RelativeRope(rot_dims=w.head_dim, base=ROPE_BASE))
+    Lr.Kc.copy_(L.Kc)
+    Lr.Vc.copy_(L.Vc)
+    Lr.S.copy_(L.S)
+    Lr.z.copy_(L.z)
+    Lr.frames = L.frames
+
+    def rope_step(stream):
+        Lr.absorb_slots(evict_slot, w.chunk_frames, stream)
+        Lr.forward(Q, O, idx, stream)
+    ms_rstep = time_graph(rope_step, dev, flush, n)
+    Lr.check_device_status()
+    out["step_with_rope"] = {"ms_per_step": ms_rstep, "us_per_latent_frame": 1000 * ms_rstep / w.chunk_frames,
+                             "vs_step": ms_rstep / step_ms,
+                             "how": "layer.step's forward with RelativeRope(rot_dims=d, base 10000, bound W-1): absorb, "
+                                    "RoPE of the window keys and chunk queries, key pooling of the 9 rotated frames, "
+                                    "prologue, attention; one CUDA graph, L2 flushed before each replay"}
+    del Lr
+
     wd = CONFIGS["dense_w21"]
     cfg_d = hb.make_config(wd.batch, wd.heads, wd.head_dim, wd.tokens_per_frame, wd.window_frames,
                            wd.chunk_frames, wd.block_size, wd.k_for(0))

@@ -14,21 +14,39 @@ window.  Logical window order (oldest first) is passed as the slot map, so
 no frame is ever moved.  Frame f lives in slot f mod R.
 
 With spare_slots = C the next chunk's keys/values can be copied in while the
-current chunk's forward still reads the window (HostStreamer below).  The C
+current chunk's forward still reads the window (HostStreamer below).  With a
+RelativeRope the forward first rotates the window's keys into a copy and the
+chunk's queries by their window-relative offsets (the ring keeps the
+unrotated keys for the absorb).  The C
 ABI sees a ring of R slots (its config's window_frames = R) and a window of
 n_win <= W frames; the top-K count is the config's fixed topk.
 """
 
 from __future__ import annotations
 
+from dataclasses import dataclass
 
 import torch
 
 from . import binding as hb
 
 
+@dataclass(frozen=True)
+class RelativeRope:
+    """The relative temporal RoPE of the layer (English technical summary,
+    section 2.C: temporal RoPE indices are window-relative and held under one
+    fixed bound).  Each forward rotates the chunk's queries and the window's
+    keys by their frame's offset inside the current window (oldest frame 0),
+    clamped to max_offset (None: the window's largest offset, W - 1); values
+    and the linear state are not rotated."""
+    rot_dims: int
+    base: float = 10000.0
+    max_offset: int | None = None
+
+
 class HybridAttentionLayer:
-    def __init__(self, cfg: hb.HFConfig, device="cuda", slot_stride: int | None = None, spare_slots: int = 0):
+    def __init__(self, cfg: hb.HFConfig, device="cuda", slot_stride: int | None = None, spare_slots: int = 0,
+                 rope: RelativeRope | None = None):
         self.window = cfg.window_frames                  # W: frames attended (chunk included)
         self.R = cfg.window_frames + spare_slots         # ring slots
         self.cfg = hb.HFConfig.from_buffer_copy(cfg)     # the ABI's view: window_frames = ring slots
@@ -48,6 +66,11 @@ class HybridAttentionLayer:
         self.frames = 0
         # ring slots whose pooled key blocks are in the workspace's cache (host bookkeeping)
         self.pooled: set[int] = set()
+        # with RoPE: the window's keys rotated for the current step (the ring keeps
+        # the unrotated keys, which the absorb reads), and the chunk's rotated queries
+        self.rope = rope
+        self.Kr = torch.zeros_like(self.Kc) if rope is not None else None
+        self.Qr: torch.Tensor | None = None
 
     # ---- window bookkeeping (host) ----
     def n_win(self) -> int:
@@ -92,10 +115,14 @@ class HybridAttentionLayer:
 
     def write_chunk(self, K_new: torch.Tensor, V_new: torch.Tensor, stream=None):
         """K_new, V_new: contiguous [BH, C, N_f, d] bf16 for the next C frames.
-        The chunk's key blocks are pooled into the cache right after the copy."""
+        The chunk's key blocks are pooled into the cache right after the copy
+        (with RoPE the forward pools the rotated window instead)."""
         slots = self.chunk_slots()
         hb.hf_ring_write(self.cfg, K_new, V_new, self.Kc, self.Vc, self.ss, slots, stream)
-        self.pool_slots(slots, stream)
+        if self.rope is None:
+            self.pool_slots(slots, stream)
+        else:
+            self.invalidate_key_cache(slots)
         self.frames += self.C
 
     def pool_slots(self, slots, stream=None):
@@ -116,10 +143,40 @@ class HybridAttentionLayer:
         Uses the cached key pools when every window slot is in the cache;
         otherwise pools the whole window (which fills the cache)."""
         sm = self.slot_map()
+        if self.rope is not None:
+            self._forward_rope(Q, O, idx_out, stream, events)
+            return
         cached = all(sl in self.pooled for sl in sm)
         hb.hf_hybrid_forward_ex(self.cfg, Q, self.Kc, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O, idx_out,
                                 self.ws, hb.HF_FWD_CACHED_KEYS if cached else 0, events, stream)
         self.pooled.update(sm)
+
+    def rope_offsets(self) -> tuple[list[int], list[int], int]:
+        """(key offsets of the window's frames in logical order, query offsets
+        of the chunk's frames, the bound) for the current window."""
+        n = self.n_win()
+        bound = self.rope.max_offset if self.rope.max_offset is not None else self.window - 1
+        return list(range(n)), list(range(n - self.C, n)), bound
+
+    def _forward_rope(self, Q, O, idx_out, stream, events):
+        """Rotate the window's keys (ring -> rotated copy) and the chunk's
+        queries by their window-relative offsets, pool the rotated window's key
+        blocks (every frame's offset moved with the window), then the forward
+        on the rotated keys and queries and the unrotated values."""
+        r = self.rope
+        sm = self.slot_map()
+        k_off, q_off, bound = self.rope_offsets()
+        if self.Qr is None or self.Qr.shape != Q.shape:
+            self.Qr = torch.empty_like(Q)
+        nfd = self.nf * self.d
+        hb.hf_rope_relative(self.cfg, self.Kc, self.Kr, self.R * self.ss * self.d, self.ss * self.d, sm, k_off, bound,
+                            r.rot_dims, r.base, stream)
+        hb.hf_rope_relative(self.cfg, Q, self.Qr, self.C * nfd, nfd, list(range(self.C)), q_off, bound, r.rot_dims,
+                            r.base, stream)
+        hb.hf_pool_keys(self.cfg, self.Kr, self.ss, sm, self.ws, stream)
+        hb.hf_hybrid_forward_ex(self.cfg, self.Qr, self.Kr, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O,
+                                idx_out, self.ws, hb.HF_FWD_CACHED_KEYS, events, stream)
+        self.pooled.clear()   # the cache holds this step's rotated pools
 
     def step(self, Q, K_new, V_new, O, idx_out=None, stream=None):
         self.absorb_evicted(stream)

@@ -8,8 +8,11 @@ import torch
 
 import oracle
 from hybrid_sparse_linear_scores_b300 import binding as hb
+from hybrid_sparse_linear_scores_b300 import synth
+from hybrid_sparse_linear_scores_b300.stream import HybridAttentionLayer, RelativeRope
+from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, Workload, frames_tensor
 
-from gpu_harness import compare
+from gpu_harness import compare, config_of, flat
 
 pytestmark = pytest.mark.gpu
 
@@ -72,3 +75,52 @@ def test_rope_ring_layout(cuda_device):
     untouched[slots] = False
     assert torch.all(out[:, untouched] == 3.0)
     assert torch.all(out[:, :, nf:] == 3.0)
+
+
+ROPE_STREAMS = {
+    "tiny": CONFIGS["tiny"],
+    "d128_b64_ragged": Workload("rope_s", 1, 2, 128, 200, 3, 9, 64, seed=31, recipe="drift", topk_frac=0.25, steps=5),
+}
+
+
+@pytest.mark.parametrize("name", list(ROPE_STREAMS))
+def test_layer_step_with_relative_rope(name, cuda_device):
+    """layer.step with the relative RoPE on, streamed until frames are
+    evicted: every step's rotated window keys and chunk queries against the
+    oracle's rope_relative (window-relative offsets, bound W - 1), and the
+    step's selection (bit-exact) and output against the oracle's forward on
+    those rotated tensors, with the state built from the unrotated evicted
+    keys (the linear state is not rotated)."""
+    w = ROPE_STREAMS[name]
+    rot = w.head_dim - 16 if w.head_dim > 64 else w.head_dim
+    cfg = config_of(w, w.steps - 1)
+    layer = HybridAttentionLayer(cfg, cuda_device, rope=RelativeRope(rot_dims=rot))
+    BH, nf, d, C = w.heads_total, w.tokens_per_frame, w.head_dim, w.chunk_frames
+    for s in range(w.steps):
+        layer.cfg.topk = w.k_for(s)
+        Kn = frames_tensor(w, synth.STREAM_K, w.chunk(s), cuda_device)
+        Vn = frames_tensor(w, synth.STREAM_V, w.chunk(s), cuda_device)
+        Q = flat(frames_tensor(w, synth.STREAM_Q, w.chunk(s), cuda_device))
+        O = torch.empty_like(Q)
+        idx = torch.empty((BH, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+        layer.step(Q, Kn, Vn, O, idx)
+        torch.cuda.synchronize()
+        layer.check_device_status()
+        k_off, q_off, bound = layer.rope_offsets()
+        assert bound == w.window_frames - 1 and k_off == list(range(w.n_win(s)))
+        win = w.window(s)
+        K_unrot = frames_tensor(w, synth.STREAM_K, win)
+        Kr = layer.Kr[:, layer.slot_map(), :nf]                      # [BH, n_win, N_f, d], logical order
+        compare(Kr, oracle.rope_relative(K_unrot, k_off, bound, rot), what=f"{name} step {s} keys")
+        Qr = layer.Qr.reshape(BH, C, nf, d)
+        compare(Qr, oracle.rope_relative(Q.reshape(BH, C, nf, d).cpu(), q_off, bound, rot),
+                what=f"{name} step {s} queries")
+        ev = list(range(w.absorbed_before(s)))
+        S = z = None
+        if ev:
+            S, z = oracle.state_from_frames(flat(frames_tensor(w, synth.STREAM_K, ev)),
+                                            flat(frames_tensor(w, synth.STREAM_V, ev)))
+        ref = oracle.hybrid_forward(layer.Qr.cpu(), flat(Kr).cpu(), flat(frames_tensor(w, synth.STREAM_V, win)), S,
+                                    z, C=C, n_win=w.n_win(s), nf=nf, beta=w.block_size, k=w.k_for(s))
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"], err_msg=f"{name} step {s}")
+        compare(O, ref["O"], what=f"{name} step {s}")
