@@ -516,6 +516,103 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
     return out
 
 
+def forward_breakdown(L, Q, O, idx, dev, flush, n):
+    """Mean ms of the layer's forward (cached key pools) as one CUDA graph, and
+    of its prologue and attention kernels (external event records between
+    them), L2 flushed before each replay."""
+    cap = torch.cuda.Stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    stream = torch.cuda.current_stream(dev)
+    for e in ev:
+        e.record(stream)
+    with torch.cuda.stream(cap):
+        L.forward(Q, O, idx, cap)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        L.forward(Q, O, idx, torch.cuda.current_stream(dev), ev)
+    torch.cuda.synchronize()
+    pro, att = [], []
+    for i in range(n + 3):
+        flush.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= 3:
+            pro.append(ev[1].elapsed_time(ev[2]))
+            att.append(ev[2].elapsed_time(ev[3]))
+    total = time_graph(lambda st: L.forward(Q, O, idx, st), dev, flush, n)
+    return total, statistics.mean(pro), statistics.mean(att)
+
+
+def workload_figures(dev, flush, n):
+    """Secondary figures on the other workloads of the same layer shape: the
+    sparsity/block sweep (top-K 10/25/50/100 % of the window's key blocks,
+    blocks of 64 and 128 tokens, clustered keys) and the 40-head layer.  Per
+    workload: the forward with cached key pools (prologue + attention) per
+    latent frame, and the attention kernel's effective TFLOP/s and fraction of
+    the measured bf16 peak; for the 40-head layer also the whole step."""
+    from hybrid_sparse_linear_scores_b300 import binding as hb
+    from hybrid_sparse_linear_scores_b300 import synth
+    from hybrid_sparse_linear_scores_b300.workloads import CONFIGS, SWEEP, frames_tensor
+    pk = peaks()
+    out = {"sweep": [], "wide": None}
+    flat = lambda x: x.reshape(x.shape[0], -1, x.shape[-1])
+    for w in list(SWEEP) + [CONFIGS["wide"]]:
+        cfg = hb.make_config(w.batch, w.heads, w.head_dim, w.tokens_per_frame, w.window_frames, w.chunk_frames,
+                             w.block_size, w.k_for(0))
+        L, _, _ = build_layer(w, cfg, dev)
+        Q = flat(frames_tensor(w, synth.STREAM_Q, w.chunk(0), dev))
+        O = torch.empty_like(Q)
+        idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(0)), dtype=torch.int32, device=dev)
+        L.forward(Q, O, idx)                      # pools the window into the cache
+        torch.cuda.synchronize()
+        fwd_ms, pro_ms, att_ms = forward_breakdown(L, Q, O, idx, dev, flush, n)
+        L.check_device_status()
+        n_ev = w.chunk_frames * w.tokens_per_frame
+        fl = step_flops(w, idx.cpu().numpy(), n_ev)
+        att_tf = (fl["attn"] + fl["lin"]) / (att_ms * 1e-3) / 1e12
+        rec = {"workload": workload_desc(w), "forward_ms": fwd_ms,
+               "forward_us_per_latent_frame": 1000 * fwd_ms / w.chunk_frames,
+               "prologue_ms": pro_ms, "attention_ms": att_ms, "attention_tflops": att_tf,
+               "attention_frac": att_tf / pk["bf16_tflops"], "attention_gflop": (fl["attn"] + fl["lin"]) / 1e9}
+        if w.name == "wide":
+            first = w.window(0)[0] % L.R
+            slots = [f % L.R for f in w.chunk(0)]
+
+            def step(stream):
+                L.absorb_slots(first, w.chunk_frames, stream)
+                L.pool_slots(slots, stream)
+                L.forward(Q, O, idx, stream)
+            ms = time_graph(step, dev, flush, n)
+            L.check_device_status()
+            rec.update({"step_ms": ms, "step_us_per_latent_frame": 1000 * ms / w.chunk_frames,
+                        "step_tflops": fl["total"] / (ms * 1e-3) / 1e12})
+            out["wide"] = rec
+        else:
+            out["sweep"].append(rec)
+        del L
+        torch.cuda.synchronize()
+    return out
+
+
+def pinned_h2d_rate(dev, nbytes: int = 43130880, n: int = 20):
+    """GB/s of one plain copy of nbytes from pinned host memory to the device
+    (the size of a chunk's Q, K and V), CUDA events on the copying stream."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(dev)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            d.copy_(h, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(n):
+            d.copy_(h, non_blocking=True)
+        e1.record(st)
+    torch.cuda.synchronize()
+    return nbytes * n / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
 def run_hf(args):
     ws, rank, local = dist_env()
     dev = torch.device("cuda", local)
@@ -651,9 +748,12 @@ def run_hf(args):
         streamer.synchronize()
         e2e_ms = max_over_ranks(1000 * (time.perf_counter() - t0) / n_e2e, ws, dev)
         L2.check_device_status()
+        h2d_step = (streamer.h2d_bytes - b0) // n_e2e
         e2e = {"value": job_throughput(fl["total"], ws, e2e_ms), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": (streamer.h2d_bytes - b0) // n_e2e,
+               "h2d_bytes_per_step": h2d_step,
                "d2h_bytes_per_step": (streamer.d2h_bytes - d0) // n_e2e, "ms_per_step": e2e_ms,
+               "h2d_GB_s_implied": h2d_step / (e2e_ms * 1e-3) / 1e9,
+               "h2d_GB_s_plain_pinned_copy": pinned_h2d_rate(dev, int(h2d_step)),
                "how": "HostStreamer: per chunk, Q and the chunk's K/V copied from pinned host memory and O "
                       "copied back, on copy streams overlapped with the neighbouring chunks' compute; "
                       f"host wall clock over {n_e2e} chunks"}
@@ -667,6 +767,11 @@ def run_hf(args):
         except Exception as exc:   # noqa: BLE001 - reported, not swallowed
             print(f"bench: extra measurements failed: {exc!r}", file=sys.stderr, flush=True)
             extra = {"extras_error": repr(exc)}
+        try:
+            extra["workloads"] = workload_figures(dev, flush, min(args.steps, 50))
+        except Exception as exc:   # noqa: BLE001 - reported, not swallowed
+            print(f"bench: workload figures failed: {exc!r}", file=sys.stderr, flush=True)
+            extra["workloads_error"] = repr(exc)
         torch.cuda.synchronize()
         L.check_device_status()
 
