@@ -184,7 +184,7 @@ enum {
     M_TMEM = 0,
     M_ABORT = 1,
     M_NLIST = 2,
-    M_LAST = 3,      // 2: last list position (+1) that each tile needs
+    M_CAT = 22,      // 3: slabs needed by both tiles / by tile A only / by tile B only
     M_WCOUNT = 8,    // 4: per-warp counts of the list compaction
     M_PFIRST = 12,   // split mode: the CTA's first pair, and
     M_PREF = 13,     //   the global round at which that pair starts
@@ -434,8 +434,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_init(&bar[B_LIN_FULL], 1);
                 mbar_init(&bar[B_DRAIN], 1);
-                misc[M_LAST] = 0;
-                misc[M_LAST + 1] = 0;
                 fence_mbar_init();
                 // the Q tiles depend only on the pair, so they load while the list is built
                 // (the previous pair's output store has finished reading the Q region)
@@ -503,28 +501,78 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = tid + 128; i < total[t]; i += 128) mark(t, i, __ldg(ip[t] + i));
             }
             bar_ctl();
-            {   // ordered compaction of the slabs that either tile needs
-                int base_out = 0;
+            {   // The slabs that either tile needs, ordered so that the rounds (pairs of
+                // consecutive list entries) keep both tiles busy: (1) slabs both tiles
+                // need, two per round; (2) rounds of two slabs only tile A needs
+                // alternating with rounds of two only tile B needs, so that one tile's
+                // softmax runs while the tensor core works on the other tile; (3) the
+                // rest of the longer side; (4) the odd slab of (1), if any.  Window
+                // order within each group.  The count of rounds is ceil(n / 2) as in
+                // any order.
+                auto cat_of = [](uint32_t m) -> int {
+                    return m == 0u ? 0 : ((m & 0x00FFu) && (m & 0xFF00u)) ? 1 : ((m & 0x00FFu) ? 2 : 3);
+                };
+                if (tid < 3) misc[M_CAT + tid] = 0;
+                bar_ctl();
+                {
+                    int c1 = 0, c2 = 0, c3 = 0;
+                    for (int s = tid; s < nsl; s += 128) {
+                        const int c = cat_of((sMask[s >> 1] >> ((s & 1) * 16)) & 0xFFFFu);
+                        c1 += c == 1;
+                        c2 += c == 2;
+                        c3 += c == 3;
+                    }
+                    c1 = __reduce_add_sync(0xFFFFFFFFu, c1);
+                    c2 = __reduce_add_sync(0xFFFFFFFFu, c2);
+                    c3 = __reduce_add_sync(0xFFFFFFFFu, c3);
+                    if (lane == 0) {
+                        atomicAdd(&misc[M_CAT + 0], (uint32_t)c1);
+                        atomicAdd(&misc[M_CAT + 1], (uint32_t)c2);
+                        atomicAdd(&misc[M_CAT + 2], (uint32_t)c3);
+                    }
+                }
+                bar_ctl();
+                const int nI = (int)misc[M_CAT], nA = (int)misc[M_CAT + 1], nB = (int)misc[M_CAT + 2];
+                const int base_out = nI + nA + nB;
+                const int nI2 = nI & ~1;
+                const int mp = 2 * min(nA >> 1, nB >> 1);   // slabs of each side in the alternating part
+                int run[3] = {0, 0, 0};                     // slabs of each group placed by earlier chunks
                 for (int base = 0; base < nsl; base += 128) {
                     const int s = base + tid;
                     const uint32_t m = s < nsl ? (sMask[s >> 1] >> ((s & 1) * 16)) & 0xFFFFu : 0u;
-                    const uint32_t ball = __ballot_sync(0xFFFFFFFFu, m != 0);
-                    if (lane == 0) misc[M_WCOUNT + warp] = __popc(ball);
+                    const int cat = cat_of(m);
+                    uint32_t ball[3];
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) ball[k] = __ballot_sync(0xFFFFFFFFu, cat == k + 1);
+                    if (lane == 0)
+                        misc[M_WCOUNT + warp] = (uint32_t)__popc(ball[0]) | ((uint32_t)__popc(ball[1]) << 8) |
+                                                ((uint32_t)__popc(ball[2]) << 16);
                     bar_ctl();
-                    int before = base_out, tot = 0;
+                    int before[3] = {run[0], run[1], run[2]}, tot[3] = {0, 0, 0};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int c = (int)misc[M_WCOUNT + q];
-                        if (q < warp) before += c;
-                        tot += c;
+                        const uint32_t w = misc[M_WCOUNT + q];
+#pragma unroll
+                        for (int k = 0; k < 3; ++k) {
+                            const int c = (int)((w >> (8 * k)) & 0xFFu);
+                            if (q < warp) before[k] += c;
+                            tot[k] += c;
+                        }
                     }
-                    if (m != 0) {
-                        const int pos = before + __popc(ball & ((1u << lane) - 1u));
+                    if (cat != 0) {
+                        const int k = cat - 1;
+                        const int q = before[k] + __popc(ball[k] & ((1u << lane) - 1u));
+                        int pos;
+                        if (k == 0)
+                            pos = q < nI2 ? q : base_out - 1;
+                        else if (k == 1)
+                            pos = q < mp ? nI2 + 2 * (q & ~1) + (q & 1) : nI2 + mp + q;
+                        else
+                            pos = q < mp ? nI2 + 2 * (q & ~1) + 2 + (q & 1) : nI2 + nA + q;
                         sList[pos] = static_cast<uint32_t>(s) | (m << 16);
-                        if (m & 0x00FFu) atomicMax(&misc[M_LAST + 0], (uint32_t)pos + 1u);
-                        if (m & 0xFF00u) atomicMax(&misc[M_LAST + 1], (uint32_t)pos + 1u);
                     }
-                    base_out += tot;
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) run[k] += tot[k];
                     bar_ctl();
                 }
                 if (tid == 0) {
@@ -681,25 +729,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (r == (t ? last_round1 : last_round0)) mma_commit_warp(&bar[B_O_DONE + t]);
                     return true;
                 };
-                // round codes are read one round ahead of their use
-                uint32_t c_cur = sCode[ra];
-                uint32_t c_nxt = ra + 1 < rb ? sCode[ra + 1] : 0u;
-                if (ok) ok = issue_qk(ra, 0, tile_bits(c_cur, 0)) && issue_qk(ra, 1, tile_bits(c_cur, 1));
-                if (ok) mma_commit_warp(&bar[B_K_EMPTY + 0]);
-                for (int r = ra; ok && r < rb; ++r) {
-                    const uint32_t c_nn = r + 2 < rb ? sCode[r + 2] : 0u;
+                // One loop body for every batch, so that each batch's code exists once
+                // (the issuer then runs from a small stretch of code): for r = ra - 1
+                // .. rb - 1 and t = A, B: P V_t(r) (r >= ra), then Q K^T_t(r + 1)
+                // (r + 1 < rb).  Round codes are read one round ahead of their use.
+                uint32_t c_cur = 0u;
+                uint32_t c_nxt = ra < rb ? sCode[ra] : 0u;
+#pragma unroll 1
+                for (int r = ra - 1; ok && r < rb; ++r) {
                     const bool more = r + 1 < rb;
-                    ok = issue_pv(r, 0, tile_bits(c_cur, 0));
-                    if (ok && more) ok = issue_qk(r + 1, 0, tile_bits(c_nxt, 0));
-                    if (ok) ok = issue_pv(r, 1, tile_bits(c_cur, 1));
-                    if (!ok) break;
-                    mma_commit_warp(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
-                    if (more) {
-                        ok = issue_qk(r + 1, 1, tile_bits(c_nxt, 1));
-                        if (ok) mma_commit_warp(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
+#pragma unroll 1
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (r >= ra) {
+                            ok = issue_pv(r, t, tile_bits(c_cur, t));
+                            if (ok && t == 1) mma_commit_warp(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
+                        }
+                        if (ok && more) {
+                            ok = issue_qk(r + 1, t, tile_bits(c_nxt, t));
+                            if (ok && t == 1) mma_commit_warp(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
+                        }
                     }
                     c_cur = c_nxt;
-                    c_nxt = c_nn;
+                    c_nxt = r + 2 < rb ? sCode[r + 2] : 0u;
                 }
                 if (FUSED && ok) {
                     ok = wait_all(&bar[B_LIN_FULL], 0, SITE_ATTN_LIN);
@@ -965,20 +1016,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float l_own = participated ? l_tot : 0.0f;
                         if (participated) tc_fence_after();
 #pragma unroll 1
-                        for (int cb = 0; cb < D; cb += 64) {
-                            uint32_t o[2][32];
+                        for (int cb = 0; cb < D; cb += 32) {
+                            uint32_t o[32];
                             if (participated) {
-                                tmem_ld32_nw(o_col + cb, o[0]);
-                                tmem_ld32_nw(o_col + cb + 32, o[1]);
+                                tmem_ld32_nw(o_col + cb, o);
                                 tmem_wait_ld();
-                                reg_dep32(o[0]);
-                                reg_dep32(o[1]);
+                                reg_dep32(o);
                             } else {
 #pragma unroll
-                                for (int c = 0; c < 32; ++c) o[0][c] = o[1][c] = 0u;
+                                for (int c = 0; c < 32; ++c) o[c] = 0u;
                             }
 #pragma unroll
-                            for (int c = 0; c < 64; ++c) __stcg(mine + (cb + c) * 128, __uint_as_float(o[c >> 5][c & 31]));
+                            for (int c = 0; c < 32; ++c) __stcg(mine + (cb + c) * 128, __uint_as_float(o[c]));
                         }
                         __stcg(mine + D * 128, m_own);
                         __stcg(mine + (D + 1) * 128, l_own);
@@ -999,49 +1048,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float sc_own = scale_of(m_own);
                             float lt = 0.0f;
 #pragma unroll 1
-                            for (int cb = 0; cb < D; cb += 64) {
-                                float acc[64];
+                            for (int cb = 0; cb < D; cb += 32) {
+                                float acc[32];
 #pragma unroll
-                                for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+                                for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+#pragma unroll 1
                                 for (int c = c0; c <= c1; ++c) {
                                     if (!share_nonempty(c, T, G)) continue;
                                     float sc, lk;
-                                    float v[64];
+                                    uint32_t v[32];
                                     if (c == me) {
-                                        uint32_t o[2][32];
                                         if (participated) {
-                                            tmem_ld32_nw(o_col + cb, o[0]);
-                                            tmem_ld32_nw(o_col + cb + 32, o[1]);
+                                            tmem_ld32_nw(o_col + cb, v);
                                             tmem_wait_ld();
-                                            reg_dep32(o[0]);
-                                            reg_dep32(o[1]);
+                                            reg_dep32(v);
                                         } else {
 #pragma unroll
-                                            for (int k = 0; k < 32; ++k) o[0][k] = o[1][k] = 0u;
+                                            for (int k = 0; k < 32; ++k) v[k] = 0u;
                                         }
-#pragma unroll
-                                        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(o[k >> 5][k & 31]);
                                         sc = sc_own;
                                         lk = l_own;
                                     } else {
                                         const float* src = part_col(c);
 #pragma unroll
-                                        for (int k = 0; k < 64; ++k) v[k] = __ldcg(src + (cb + k) * 128);
+                                        for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__ldcg(src + (cb + k) * 128));
                                         const float mk = __ldcg(src + D * 128);
                                         lk = __ldcg(src + (D + 1) * 128);
                                         sc = scale_of(mk);
                                     }
                                     if (cb == 0) lt = fmaf(sc, lk, lt);
 #pragma unroll
-                                    for (int k = 0; k < 64; ++k) acc[k] = fmaf(sc, v[k], acc[k]);
+                                    for (int k = 0; k < 32; ++k) acc[k] = fmaf(sc, __uint_as_float(v[k]), acc[k]);
                                 }
                                 uint32_t o[32];
 #pragma unroll
-                                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc[32 * h + k]);
-                                    tmem_st32(o_col + cb + 32 * h, o);
-                                }
+                                for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc[k]);
+                                tmem_st32(o_col + cb, o);
                             }
                             l_tot = lt;
                             tc_fence_before();
@@ -1105,30 +1147,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
                             const float inv_den = 1.0f / den;
 #pragma unroll 1
-                            for (int cb = 0; cb < D; cb += 64) {
-                                uint32_t o[2][32], li[2][32];
-                                tmem_ld32_nw(o_col + cb, o[0]);
-                                tmem_ld32_nw(o_col + cb + 32, o[1]);
-                                tmem_ld32_nw(s_col + cb, li[0]);
-                                tmem_ld32_nw(s_col + cb + 32, li[1]);
+                            for (int cb = 0; cb < D; cb += 32) {
+                                uint32_t o[32], li[32];
+                                tmem_ld32_nw(o_col + cb, o);
+                                tmem_ld32_nw(s_col + cb, li);
                                 tmem_wait_ld();
-                                reg_dep32(o[0]);
-                                reg_dep32(o[1]);
-                                reg_dep32(li[0]);
-                                reg_dep32(li[1]);
+                                reg_dep32(o);
+                                reg_dep32(li);
                                 uint8_t* rowp = sQ + (cb >> 6) * (Cfg::TILE_M * 128) + r * 128;
 #pragma unroll
-                                for (int ch = 0; ch < 8; ++ch) {   // logical 16-byte chunks of the row
+                                for (int cq = 0; cq < 4; ++cq) {   // 16-byte chunks of the row
+                                    const int ch = ((cb >> 3) & 7) + cq;
                                     uint32_t w4[4];
 #pragma unroll
                                     for (int i = 0; i < 4; ++i) {
-                                        const int c = (ch & 3) * 8 + 2 * i;
-                                        const uint32_t* oh = o[ch >> 2];
-                                        const uint32_t* lh = li[ch >> 2];
+                                        const int c = cq * 8 + 2 * i;
                                         const float a =
-                                            fmaf(__uint_as_float(oh[c]), inv_l, __uint_as_float(lh[c]) * inv_den);
-                                        const float bq = fmaf(__uint_as_float(oh[c + 1]), inv_l,
-                                                              __uint_as_float(lh[c + 1]) * inv_den);
+                                            fmaf(__uint_as_float(o[c]), inv_l, __uint_as_float(li[c]) * inv_den);
+                                        const float bq = fmaf(__uint_as_float(o[c + 1]), inv_l,
+                                                              __uint_as_float(li[c + 1]) * inv_den);
                                         w4[i] = pack_bf16(a, bq);
                                     }
                                     *reinterpret_cast<uint4*>(rowp + (((ch ^ (r & 7)) & 7) << 4)) =
