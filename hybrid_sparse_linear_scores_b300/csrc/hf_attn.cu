@@ -693,10 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         k_desc + (uint64_t)((s * Cfg::RS_BYTES + (m == 2u ? Cfg::SLAB * 128 : 0)) >> 4);
                     const uint32_t idesc = m == 3u ? Cfg::IDESC_QK128 : Cfg::IDESC_QK64;
                     const uint32_t dt = tmem + 256 * t + 128;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss_warp(dt, qd + (uint64_t)(((kk >> 2) * (Cfg::TILE_M * 128) + (kk & 3) * 32) >> 4),
-                               kd + (uint64_t)(((kk >> 2) * Cfg::CHUNK + (kk & 3) * 32) >> 4), idesc, kk > 0 ? 1u : 0u);
+                    static_assert(D == 64 || Cfg::TILE_M * 128 == Cfg::CHUNK, "one chunk stride for Q and K");
+                    mma_ss_kloop_warp<D / 16, (Cfg::CHUNK >> 4)>(dt, qd, kd, idesc, 0u);
                     mma_commit_warp(&bar[B_S_FULL + t]);
                     return true;
                 };
@@ -720,10 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int i = (m == 2u) ? 1 : j;   // slab of the round; P columns [32j, 32j + 32)
                         const uint64_t vd = v_desc + (uint64_t)((s * Cfg::RS_BYTES + i * Cfg::SLAB * 128) >> 4);
                         const uint32_t at = o_tm + 128 + 32 * j;
-#pragma unroll
-                        for (int kk = 0; kk < Cfg::SLAB / 16; ++kk)
-                            mma_ts_warp(o_tm, at + kk * 8, vd + (uint64_t)(kk * (2048 >> 4)), Cfg::IDESC_PV,
-                                   (first && j == 0 && kk == 0) ? 0u : 1u);
+                        static_assert(Cfg::SLAB / 16 == 4, "four K steps per slab");
+                        mma_ts_k4_warp<(2048 >> 4)>(o_tm, at, vd, Cfg::IDESC_PV, (first && j == 0) ? 0u : 1u);
                     }
                     first = false;
                     if (r == (t ? last_round1 : last_round0)) mma_commit_warp(&bar[B_O_DONE + t]);

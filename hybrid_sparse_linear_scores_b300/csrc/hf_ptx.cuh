@@ -218,6 +218,76 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// A whole K loop of tcgen05.mma (kind::f16, cta_group::1) in one block,
+// issued by one elected lane of a converged warp.  A and B are K-major with
+// the 128-byte swizzle: 16-element K steps are 32 bytes (2 descriptor units)
+// apart inside a 64-element chunk, chunks CH descriptor units apart.  The
+// first MMA accumulates into D iff `acc`, the others always.  NK = 4 or 8.
+template <int NK, int CH>
+__device__ __forceinline__ void mma_ss_kloop_warp(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    static_assert(NK == 4 || NK == 8, "K loop of 4 or 8 steps");
+    if (NK == 4) {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t}"
+            ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(1u)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred e, p, t;\n\t.reg .b64 ra, rb;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+            "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, %6;\n\tadd.s64 rb, %2, %6;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, %7;\n\tadd.s64 rb, %2, %7;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, %8;\n\tadd.s64 rb, %2, %8;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t"
+            "add.s64 ra, %1, %9;\n\tadd.s64 rb, %2, %9;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, t;\n\t}"
+            ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(1u), "n"(CH), "n"(CH + 2), "n"(CH + 4), "n"(CH + 6)
+            : "memory");
+    }
+}
+
+// Four tcgen05.mma with A from tensor memory (16 K elements = 8 columns per
+// step) and B from shared memory (K steps STEP descriptor units apart), in
+// one block, issued by one elected lane of a converged warp.  The first
+// accumulates iff `acc`.
+template <int STEP>
+__device__ __forceinline__ void mma_ts_k4_warp(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p, t;\n\t.reg .b64 rb;\n\t.reg .b32 ra;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 t, %5, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+        "add.u32 ra, %1, 8;\n\tadd.s64 rb, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+        "add.u32 ra, %1, 16;\n\tadd.s64 rb, %2, %7;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t"
+        "add.u32 ra, %1, 24;\n\tadd.s64 rb, %2, %8;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ra], rb, %3, t;\n\t}"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(1u), "n"(STEP), "n"(2 * STEP), "n"(3 * STEP)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar)
 {
     asm volatile(
