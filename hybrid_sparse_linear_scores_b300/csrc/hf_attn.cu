@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int t = 0; t < 2; ++t) {
                     mbar_init(&bar[B_S_FULL + t], 1);
-                    mbar_init(&bar[B_P_FULL + t], 128);
+                    mbar_init(&bar[B_P_FULL + t], 4);   // one arrival per softmax warp
                     mbar_init(&bar[B_O_DONE + t], 1);
                     mbar_init(&bar[B_PHIQ + t], 128);
                     mbar_init(&bar[B_LIN_DONE + t], 1);
@@ -886,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tmem_wait_st();
                         tc_fence_before();
-                        mbar_arrive(&bar[B_P_FULL + t]);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[B_P_FULL + t]);
                         continue;
                     }
                     uint32_t sr[4][32];
@@ -977,7 +978,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before();
-                    mbar_arrive(&bar[B_P_FULL + t]);
+                    __syncwarp();   // the warp's P stores are complete: one arrival for the warp
+                    if (lane == 0) mbar_arrive(&bar[B_P_FULL + t]);
                 }
                 if (ok && participated)
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_O_DONE + t], 0, wc, SITE_ATTN_PV_DONE));
