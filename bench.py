@@ -7,16 +7,18 @@ One step = the whole hot path over one chunk of the 832x480 streaming
 workload ("realistic": batch 1, 12 heads, head_dim 128, 1560 tokens per
 latent frame, 3-frame chunk, 9-frame window, block 64, top-K 25 % = 57 of
 225 key blocks, 30 frames already in the linear state):
-  hf_absorb_evicted_strided  (the 3 frames the chunk evicts, from the ring)
+  hf_absorb_evicted_strided  (the 3 frames the chunk evicts, from the ring;
+                              it also writes the state's tensor-core operand)
   hf_pool_keys               (key blocks of the chunk's 3 new frames, into
                               the pooled-key cache)
-  hf_hybrid_forward_ex       (prologue: query pooling, state operand,
-                              scores against the cached key pools, top-K;
-                              then sparse attention with the linear read
-                              and the sum fused in)
+  hf_hybrid_forward_ex       (prologue: query pooling, scores against the
+                              cached key pools, top-K; then sparse attention
+                              with the linear read and the sum fused in)
+The absorb runs on a second stream beside the key pooling and the prologue,
+which do not read the state; the attention waits for it (an event).
 Inputs are synthetic (seeded Philox, see workloads.py) and resident in HBM.
-The step is captured once as a CUDA graph (its 4 kernels, no host work in
-between) and replayed; L2 is flushed (256 MB write) before every timed
+The step is captured once as a CUDA graph (its 4 kernels on two streams, no
+host work in between) and replayed; L2 is flushed (256 MB write) before every timed
 replay, and each replay is timed with CUDA events on the launching stream.
 value = algorithmic FLOPs of the step / device time (effective TFLOP/s);
 us_per_latent_frame = time / 3.  A second graph of the same step records
@@ -115,11 +117,14 @@ def step_bytes(w, n_ev_tokens: int) -> dict:
     o = q
     ev = 2 * BH * n_ev_tokens * d * 2
     state = 2 * BH * (d * d + d) * 4
-    # the prologue reads the chunk's queries and S and writes S as the epilogue's
-    # bf16 hi/lo operand (pooled keys and indices are small and stay in L2)
-    prologue = q + BH * d * d * 4 + BH * d * d * 2 * 2
+    # the prologue reads the chunk's queries (pooled keys and indices are small and
+    # stay in L2); the absorb reads the evicted K/V and the state and writes the
+    # state and its bf16 hi/lo tensor-core operand
+    prologue = q
     pool_k = BH * w.chunk_frames * nf * d * 2   # pooling the new chunk's keys (the cache holds the rest)
-    return {"compulsory": q + kv + o + ev + state, "prologue": prologue, "pool_k": pool_k, "absorb": ev + state}
+    smma = BH * d * d * 2 * 2
+    return {"compulsory": q + kv + o + ev + state, "prologue": prologue, "pool_k": pool_k,
+            "absorb": ev + state + smma}
 
 
 class ClockSampler:
@@ -444,6 +449,7 @@ def extra_measurements(w, cfg, dev, L, Q, O, idx, evict_slot, chunk_slots, flush
     Lr.Vc.copy_(L.Vc)
     Lr.S.copy_(L.S)
     Lr.z.copy_(L.z)
+    Lr.state_changed()
     Lr.frames = L.frames
 
     def rope_step(stream):
@@ -638,16 +644,27 @@ def run_hf(args):
     n_ev = w.chunk_frames * w.tokens_per_frame
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    side = torch.cuda.Stream(dev)
+    ev_fork, ev_state = torch.cuda.Event(), torch.cuda.Event()
+
     def one_step(stream, events=None):
-        """absorb the evicted frames, pool the new chunk's key blocks, hybrid
-        forward with the other window frames' key pools from the cache."""
+        """absorb the evicted frames (on a side stream: it writes the state and
+        its tensor-core operand) beside the key pooling of the new chunk and the
+        forward's prologue (selection), which do not read the state; then the
+        attention, which waits for the absorb (as HybridAttentionLayer.step does
+        when the chunk's slots are not the evicted ones)."""
+        ev_fork.record(stream)
+        side.wait_event(ev_fork)
         if events is not None:
-            events[0].record(stream)
-        L.absorb_slots(evict_slot, w.chunk_frames, stream)
+            events[0].record(side)
+        L.absorb_slots(evict_slot, w.chunk_frames, side, share_sms=True)
         if events is not None:
-            events[1].record(stream)
+            events[1].record(side)
+        ev_state.record(side)
+        if events is not None:
+            events[2].record(stream)
         L.pool_slots(chunk_slots, stream)
-        L.forward(Q, O, idx, stream, events[2:] if events is not None else None)
+        L.forward(Q, O, idx, stream, events[3:] if events is not None else None, state_ready=ev_state)
 
     stream = torch.cuda.current_stream(dev)
     L.forward(Q, O, idx, stream)                          # fills the key-pool cache for the window
@@ -696,13 +713,14 @@ def run_hf(args):
 
     # ---- per-kernel breakdown: the same step captured with event records between
     #      its kernels (external event nodes, so they time every replay) ----
-    # events: [0] absorb [1] hf_pool_keys [2] (the forward's window key pooling: none
-    # with cached pools) [3] prologue [4] attention [5]
+    # events: [0] absorb [1] (side stream); [2] hf_pool_keys [3] (the forward's window
+    # key pooling: none with cached pools) [4] prologue [5] attention (after its wait
+    # for the absorb) [6]
     names = ["absorb", "pool_keys", "prologue", "attention"]
-    spans = {"absorb": (0, 1), "pool_keys": (1, 2), "prologue": (3, 4), "attention": (4, 5)}
+    spans = {"absorb": (0, 1), "pool_keys": (2, 3), "prologue": (4, 5), "attention": (5, 6)}
     times = {n: [] for n in names}
     n_prof = min(args.steps, 200)
-    pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+    pev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(7)]
     for e in pev:                                         # create the CUDA events before the capture
         e.record(stream)
     torch.cuda.synchronize()
@@ -791,8 +809,9 @@ def run_hf(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "l2": "flushed (256 MB write) before every step",
-                   "timing": "CUDA events around each replay of the step's CUDA graph (absorb, key pooling of "
-                             "the new chunk, hybrid forward with cached key pools (prologue + attention): 4 kernels)",
+                   "timing": "CUDA events around each replay of the step's CUDA graph (absorb on a second "
+                             "stream beside the key pooling of the new chunk and the forward's prologue; then the "
+                             "attention, which waits for the absorb: 4 kernels)",
                    "parallelism": f"replicas x{ws}"},
         "us_per_latent_frame": 1000 * ms / w.chunk_frames,
         "median_ms_per_step": statistics.median(step_ms),

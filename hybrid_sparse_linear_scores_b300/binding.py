@@ -54,7 +54,7 @@ def lib():
             "hf_workspace_size": ([cfgp, ctypes.POINTER(ctypes.c_size_t)], _I),
             "hf_state_reset": ([cfgp, _P, _P, _P], _I),
             "hf_absorb_evicted": ([cfgp, _P, _P, _P, _P, _I, _P, _P], _I),
-            "hf_absorb_evicted_strided": ([cfgp, _P, _P, _P, _P, _I, ctypes.c_int64, _P, _P], _I),
+            "hf_absorb_evicted_strided": ([cfgp, _P, _P, _P, _P, _I, ctypes.c_int64, _P, _P, ctypes.c_uint32], _I),
             "hf_block_scores": ([cfgp, _P, _P, _I, _P, _I, _P, _P, _P], _I),
             "hf_topk_blocks": ([cfgp, _P, _I, _I, _P, _P], _I),
             "hf_sparse_swa_attn": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P], _I),
@@ -65,7 +65,7 @@ def lib():
             "hf_hybrid_forward_noalloc": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P,
                                            ctypes.POINTER(ctypes.c_void_p), _P], _I),
             "hf_hybrid_forward_ex": ([cfgp, _P, _P, _P, _I, _P, _I, _P, _P, _P, _P, _P, _P, ctypes.c_uint32,
-                                      ctypes.POINTER(ctypes.c_void_p)], _I),
+                                      ctypes.POINTER(ctypes.c_void_p), _P], _I),
             "hf_pool_keys": ([cfgp, _P, _I, _P, _I, _P, _P], _I),
             "hf_ring_write": ([cfgp, _P, _P, _P, _P, _I, _P, _I, _P], _I),
             "hf_rope_relative": ([cfgp, _P, _P, ctypes.c_int64, ctypes.c_int64, _P, _P, _I, _I, _I,
@@ -137,9 +137,10 @@ def hf_absorb_evicted(cfg, S, z, K_ev, V_ev, n_ev_tokens, ws, stream=None):
                                    _ptr(ws), _stream(stream)), "hf_absorb_evicted")
 
 
-def hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, head_stride_tokens, ws, stream=None):
+def hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, head_stride_tokens, ws, stream=None, flags=0):
     _check(lib().hf_absorb_evicted_strided(ctypes.byref(cfg), _ptr(S), _ptr(z), _ptr(K_ev), _ptr(V_ev),
-                                           int(n_ev_tokens), int(head_stride_tokens), _ptr(ws), _stream(stream)),
+                                           int(n_ev_tokens), int(head_stride_tokens), _ptr(ws), _stream(stream),
+                                           ctypes.c_uint32(int(flags))),
            "hf_absorb_evicted_strided")
 
 
@@ -194,6 +195,8 @@ def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, 
 
 
 HF_FWD_CACHED_KEYS = 1
+HF_FWD_STATE_PREPARED = 2
+HF_ABSORB_SHARE_SMS = 1
 HF_FWD_EVENTS = 4
 
 
@@ -229,9 +232,11 @@ def hf_rope_relative(cfg, src, dst, head_stride, frame_stride, slots, offsets, m
 
 
 def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, flags=0, events=None,
-                         stream=None):
-    """hf_hybrid_forward with flags (HF_FWD_CACHED_KEYS) and optional per-kernel
-    events (HF_FWD_EVENTS torch.cuda.Event objects, handled as in hf_hybrid_forward_profiled)."""
+                         stream=None, state_ready=None):
+    """hf_hybrid_forward with flags (HF_FWD_CACHED_KEYS, HF_FWD_STATE_PREPARED),
+    optional per-kernel events (HF_FWD_EVENTS torch.cuda.Event objects, handled
+    as in hf_hybrid_forward_profiled) and an optional torch.cuda.Event, already
+    recorded, that the attention kernel waits for (the state's producer)."""
     st = _stream(stream)
     ev = None
     if events is not None:
@@ -242,9 +247,10 @@ def hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, 
                 e.record(ts)
         ev = (ctypes.c_void_p * HF_FWD_EVENTS)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
     sm = _slots(slot_map)
+    ready = ctypes.c_void_p(state_ready.cuda_event) if state_ready is not None else None
     _check(lib().hf_hybrid_forward_ex(ctypes.byref(cfg), _ptr(Q), _ptr(Kc), _ptr(Vc), int(slot_stride), sm and sm[0],
                                       int(n_win), _ptr(S), _ptr(z), _ptr(O), _ptr(idx_out), _ptr(ws), st,
-                                      ctypes.c_uint32(int(flags)), ev), "hf_hybrid_forward_ex")
+                                      ctypes.c_uint32(int(flags)), ev, ready), "hf_hybrid_forward_ex")
 
 
 def hf_hybrid_forward_noalloc(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, stream=None):

@@ -53,14 +53,16 @@ namespace {
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-template <int D, int NV>
+template <int D, int NV, int NSX = 0>
 struct AbsCfg {
     static constexpr int TT = 64;                    // tokens per tile
     static constexpr int CHUNK = TT * 128;           // 64 channels x 64 tokens, 128-byte swizzle: 8 KB
     static constexpr int K_BYTES = (D / 64) * CHUNK;
     static constexpr int V_BYTES = (NV / 64) * CHUNK;
     static constexpr int STAGE = K_BYTES + V_BYTES;
-    static constexpr int NS = STAGE <= 24 * 1024 ? 8 : 6;   // shared-memory stages (tiles in flight)
+    // shared-memory stages (tiles in flight); NSX > 0 chooses fewer, so that the
+    // CTA leaves room on its SM for kernels that run beside the absorb
+    static constexpr int NS = NSX > 0 ? NSX : (STAGE <= 24 * 1024 ? 8 : 6);
     static constexpr int NA = 4;                     // TMEM A-operand stages
     static constexpr int TW = 16;                    // transform warps: 4 per TMEM lane quarter
     static constexpr int TPW = TT / 4;               // tokens of a tile per transform warp
@@ -97,13 +99,14 @@ struct AbsParams {
     float* z;
     uint32_t* status;
     uint64_t wait_limit_ns;
+    uint16_t* smma;   // optional: the new S also as the linear read's bf16 hi/lo MMA operand
 };
 
-template <int D, int NV>
-__global__ void __launch_bounds__(AbsCfg<D, NV>::NTHR, 1)
+template <int D, int NV, int NSX = 0>
+__global__ void __launch_bounds__(AbsCfg<D, NV, NSX>::NTHR, 1)
     absorb_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const AbsParams p)
 {
-    using Cfg = AbsCfg<D, NV>;
+    using Cfg = AbsCfg<D, NV, NSX>;
     constexpr int NS = Cfg::NS, NA = Cfg::NA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -354,8 +357,22 @@ __global__ void __launch_bounds__(AbsCfg<D, NV>::NTHR, 1)
                     acc.w += v[q].w;
                 }
             }
-            *reinterpret_cast<float4*>(Sg + (size_t)c * D + j) =
-                make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+            const float4 nv = make_float4(old.x + acc.x, old.y + acc.y, old.z + acc.z, old.w + acc.w);
+            *reinterpret_cast<float4*>(Sg + (size_t)c * D + j) = nv;
+            if (p.smma != nullptr) {
+                // hi = rn(S), lo = rn(S - hi), MN-major with the 128-byte swizzle:
+                // per head [hi | lo][column / 64][row c][128 B], 16-byte chunks of
+                // 8 columns XOR-ed with (c mod 8); these 4 columns are one half chunk
+                const int jj = grp * NV + j;   // column of the head's state
+                const uint32_t h0 = pack_bf16(nv.x, nv.y), h1 = pack_bf16(nv.z, nv.w);
+                const uint32_t l0 = pack_bf16(nv.x - bf16_lo(h0), nv.y - bf16_hi(h0));
+                const uint32_t l1 = pack_bf16(nv.z - bf16_lo(h1), nv.w - bf16_hi(h1));
+                const uint32_t off = (uint32_t)(jj / 64) * (uint32_t)(D * 128) + (uint32_t)c * 128u +
+                                     (((((uint32_t)jj % 64u) >> 3) ^ ((uint32_t)c & 7u)) << 4) + ((uint32_t)jj & 4u) * 2u;
+                uint8_t* base = reinterpret_cast<uint8_t*>(p.smma) + (size_t)bh * 2 * D * D * 2;
+                *reinterpret_cast<uint2*>(base + off) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2*>(base + (size_t)D * D * 2 + off) = make_uint2(l0, l1);
+            }
         };
         const int total = (r1 - r0) * C4;
         if (tt >= 0) {
@@ -393,13 +410,13 @@ __global__ void __launch_bounds__(AbsCfg<D, NV>::NTHR, 1)
     }
 }
 
-template <int D, int NV>
+template <int D, int NV, int NSX = 0>
 cudaLaunchConfig_t absorb_launch_cfg(int grid, int CL, cudaStream_t st, cudaLaunchAttribute* attr)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(AbsCfg<D, NV>::NTHR);
-    cfg.dynamicSmemBytes = AbsCfg<D, NV>::SMEM_ALLOC;
+    cfg.blockDim = dim3(AbsCfg<D, NV, NSX>::NTHR);
+    cfg.dynamicSmemBytes = AbsCfg<D, NV, NSX>::SMEM_ALLOC;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CL;
@@ -410,9 +427,9 @@ cudaLaunchConfig_t absorb_launch_cfg(int grid, int CL, cudaStream_t st, cudaLaun
     return cfg;
 }
 
-// Clusters of CL CTAs of absorb_kernel<D, NV> that fit on the device at
+// Clusters of CL CTAs of absorb_kernel<D, NV, NSX> that fit on the device at
 // once (cached per device; 0 if the query fails).
-template <int D, int NV>
+template <int D, int NV, int NSX = 0>
 int max_clusters(int dev, int CL)
 {
     static std::mutex mu;
@@ -420,12 +437,12 @@ int max_clusters(int dev, int CL)
     if (dev < 0 || dev >= 64 || CL < 1 || CL > 8) return 0;
     std::lock_guard<std::mutex> lock(mu);
     if (cache[dev][CL] == 0) {
-        auto kern = absorb_kernel<D, NV>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AbsCfg<D, NV>::SMEM_ALLOC) !=
+        auto kern = absorb_kernel<D, NV, NSX>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, AbsCfg<D, NV, NSX>::SMEM_ALLOC) !=
             cudaSuccess)
             return 0;
         cudaLaunchAttribute attr[1];
-        const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV>(CL, CL, 0, attr);
+        const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV, NSX>(CL, CL, 0, attr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
@@ -436,15 +453,15 @@ int max_clusters(int dev, int CL)
     return cache[dev][CL];
 }
 
-template <int D, int NV>
+template <int D, int NV, int NSX = 0>
 int launch_absorb_t(const CUtensorMap& tk, const CUtensorMap& tv, AbsParams p, cudaStream_t st)
 {
-    using Cfg = AbsCfg<D, NV>;
-    auto kern = absorb_kernel<D, NV>;
+    using Cfg = AbsCfg<D, NV, NSX>;
+    auto kern = absorb_kernel<D, NV, NSX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_ALLOC);
     if (e != cudaSuccess) return (int)e;
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV>(p.BH * p.NG * p.CL, p.CL, st, attr);
+    const cudaLaunchConfig_t cfg = absorb_launch_cfg<D, NV, NSX>(p.BH * p.NG * p.CL, p.CL, st, attr);
     e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
     if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
@@ -455,14 +472,17 @@ int launch_absorb_t(const CUtensorMap& tk, const CUtensorMap& tv, AbsParams p, c
 // once; on ties, the larger cluster, and fewer column groups (fewer repeated
 // key reads).  Clusters of one CTA never wait on each other, so they may run
 // in several waves.
-template <int D, int NV>
+template <int D, int NV, int NSX = 0>
 void pick_shape(int BH, int n_tiles, int sms, int dev, int NG, int& best_cl, int& best_score)
 {
-    for (int CL = 8; CL >= 1; --CL) {
+    // sharing the SMs (NSX > 0): at most a third of them
+    const int max_cl = NSX > 0 ? 4 : 8;
+    if (NSX > 0) sms = (sms + 2) / 3;
+    for (int CL = max_cl; CL >= 1; --CL) {
         if (CL > n_tiles && CL > 1) continue;
         const long clusters = (long)BH * NG;
         const long ctas = clusters * CL;
-        if (CL > 1 && (ctas > sms || clusters > max_clusters<D, NV>(dev, CL))) continue;
+        if (CL > 1 && (ctas > sms || clusters > max_clusters<D, NV, NSX>(dev, CL))) continue;
         const int score = (int)(ctas < sms ? ctas : sms);
         if (score > best_score) {
             best_score = score;
@@ -471,10 +491,37 @@ void pick_shape(int BH, int n_tiles, int sms, int dev, int NG, int& best_cl, int
     }
 }
 
+
+// The shape and the launch, for one stage count (NSX: 0 = the default).
+template <int NSX>
+int launch_absorb_ns(const CUtensorMap& tk, const CUtensorMap& tv, const Geom& g, AbsParams p, int n_tiles, int sms,
+                     int dev, cudaStream_t st)
+{
+    if (g.d == 64) {
+        int cl = 1, ctas = 0;
+        pick_shape<64, 64, NSX>(g.BH, n_tiles, sms, dev, 1, cl, ctas);
+        p.CL = cl;
+        return launch_absorb_t<64, 64, NSX>(tk, tv, p, st);
+    }
+    int cl1 = 1, c1 = 0, cl2 = 1, c2 = 0;
+    pick_shape<128, 128, NSX>(g.BH, n_tiles, sms, dev, 1, cl1, c1);
+    pick_shape<128, 64, NSX>(g.BH, n_tiles, sms, dev, 2, cl2, c2);
+    // two column groups compute phi of every key twice: worth it only for
+    // clearly more CTAs
+    if (2 * c2 > 3 * c1) {
+        p.NG = 2;
+        p.CL = cl2;
+        return launch_absorb_t<128, 64, NSX>(tk, tv, p, st);
+    }
+    p.CL = cl1;
+    return launch_absorb_t<128, 128, NSX>(tk, tv, p, st);
+}
+
 }  // namespace
 
 int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int64_t head_stride, const Geom& g,
-                  float* S, float* z, uint32_t* status, uint64_t wait_limit_ns, void* stream)
+                  float* S, float* z, uint16_t* smma, bool share_sms, uint32_t* status, uint64_t wait_limit_ns,
+                  void* stream)
 {
     alignas(64) CUtensorMap tk, tv;
     const uint64_t hs = (uint64_t)head_stride * g.d * 2;
@@ -488,25 +535,12 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int n_tiles = (n_ev + TT - 1) / TT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    AbsParams p{g.BH, n_ev, 1, 1, S, z, status, wait_limit_ns};
-    if (g.d == 64) {
-        int cl = 1, ctas = 0;
-        pick_shape<64, 64>(g.BH, n_tiles, sms, dev, 1, cl, ctas);
-        p.CL = cl;
-        return launch_absorb_t<64, 64>(tk, tv, p, st);
-    }
-    int cl1 = 1, c1 = 0, cl2 = 1, c2 = 0;
-    pick_shape<128, 128>(g.BH, n_tiles, sms, dev, 1, cl1, c1);
-    pick_shape<128, 64>(g.BH, n_tiles, sms, dev, 2, cl2, c2);
-    // two column groups compute phi of every key twice: worth it only for
-    // clearly more CTAs
-    if (2 * c2 > 3 * c1) {
-        p.NG = 2;
-        p.CL = cl2;
-        return launch_absorb_t<128, 64>(tk, tv, p, st);
-    }
-    p.CL = cl1;
-    return launch_absorb_t<128, 128>(tk, tv, p, st);
+    AbsParams p{g.BH, n_ev, 1, 1, S, z, status, wait_limit_ns, smma};
+    // sharing: clusters of at most 4 CTAs on about a third of the SMs, four
+    // stages (about 130 KB of shared memory instead of 193), so that the key
+    // pooling and the forward's prologue fit beside the absorb
+    return share_sms ? launch_absorb_ns<4>(tk, tv, g, p, n_tiles, sms, dev, st)
+                     : launch_absorb_ns<0>(tk, tv, g, p, n_tiles, sms, dev, st);
 }
 
 }  // namespace hf

@@ -103,9 +103,11 @@ WsLayout ws_layout(const hf_config* cfg)
     w.counters = 1024;
     w.qp = w.counters + align1k(pairs * 2 * 4);
     w.kp = w.qp + align1k(BH * nqb * d * 4);
-    w.idx = w.kp + align1k(BH * nkb * d * 4);
-    w.smma = w.idx + align1k(BH * nqb * kmax * 4);
-    w.prounds = w.smma + align1k(BH * 2 * d * d * 2);
+    // the pooled-key cache and the state operand persist between calls, so they
+    // come before the one region whose size follows topk
+    w.smma = w.kp + align1k(BH * nkb * d * 4);
+    w.idx = w.smma + align1k(BH * 2 * d * d * 2);
+    w.prounds = w.idx + align1k(BH * nqb * kmax * 4);
     w.total_compact = w.prounds + align1k(pairs * 4);
     w.partial = w.total_compact;
     w.total = w.partial + (size_t)HF_SPLIT_PARTIAL_BYTES(d);
@@ -249,10 +251,11 @@ hf_status hf_state_reset(const hf_config* cfg, float* S, float* z, void* stream)
 
 hf_status hf_absorb_evicted_strided(const hf_config* cfg, float* S, float* z, const uint16_t* K_ev,
                                     const uint16_t* V_ev, int32_t n_ev_tokens, int64_t head_stride_tokens, void* ws,
-                                    void* stream)
+                                    void* stream, uint32_t flags)
 {
     hf_status s = check_cfg(cfg);
     if (s != HF_OK) return s;
+    if (flags & ~(uint32_t)HF_ABSORB_SHARE_SMS) return fail(HF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (n_ev_tokens < 0) return fail(HF_ERR_INVALID_ARG, "n_ev_tokens %d < 0", n_ev_tokens);
     if (head_stride_tokens < n_ev_tokens)
         return fail(HF_ERR_INVALID_ARG, "head_stride_tokens %lld < n_ev_tokens %d", (long long)head_stride_tokens,
@@ -264,8 +267,13 @@ hf_status hf_absorb_evicted_strided(const hf_config* cfg, float* S, float* z, co
     HF_CHECK_PTR(K_ev);
     HF_CHECK_PTR(V_ev);
     const Geom g = make_geom(cfg, cfg->chunk_frames, cfg->tokens_per_frame);
-    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + ws_layout(cfg).status);
-    HF_LAUNCH(launch_absorb(K_ev, V_ev, n_ev_tokens, head_stride_tokens, g, S, z, status, kDefaultWaitLimitNs, stream),
+    const WsLayout L = ws_layout(cfg);
+    uint32_t* status = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + L.status);
+    // the new S also goes to the workspace as the linear read's MMA operand, so
+    // that a forward with HF_FWD_STATE_PREPARED need not read S
+    uint16_t* smma = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + L.smma);
+    HF_LAUNCH(launch_absorb(K_ev, V_ev, n_ev_tokens, head_stride_tokens, g, S, z, smma,
+                            (flags & HF_ABSORB_SHARE_SMS) != 0, status, kDefaultWaitLimitNs, stream),
               "absorb launch");
     return HF_OK;
 }
@@ -273,7 +281,7 @@ hf_status hf_absorb_evicted_strided(const hf_config* cfg, float* S, float* z, co
 hf_status hf_absorb_evicted(const hf_config* cfg, float* S, float* z, const uint16_t* K_ev, const uint16_t* V_ev,
                             int32_t n_ev_tokens, void* ws, void* stream)
 {
-    return hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, n_ev_tokens, ws, stream);
+    return hf_absorb_evicted_strided(cfg, S, z, K_ev, V_ev, n_ev_tokens, n_ev_tokens, ws, stream, 0u);
 }
 
 hf_status hf_block_scores(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, int32_t slot_stride,
@@ -359,15 +367,17 @@ size_t compact_workspace_bytes(const hf_config* cfg) { return ws_layout(cfg).tot
 hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
                        int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S, const float* z,
                        uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags, void* const* events,
-                       bool allow_split)
+                       void* state_ready, bool allow_split)
 {
     hf_status s = check_cfg(cfg);
     if (s != HF_OK) return s;
-    if (flags & ~(uint32_t)HF_FWD_CACHED_KEYS) return fail(HF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (flags & ~(uint32_t)(HF_FWD_CACHED_KEYS | HF_FWD_STATE_PREPARED))
+        return fail(HF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    const bool prepared = (flags & HF_FWD_STATE_PREPARED) != 0;
     HF_CHECK_PTR(Q);
     HF_CHECK_PTR(Kc);
     HF_CHECK_PTR(Vc);
-    HF_CHECK_PTR(S);
+    if (!prepared) HF_CHECK_PTR(S);
     HF_CHECK_PTR(z);
     HF_CHECK_PTR(O);
     HF_CHECK_PTR(ws);
@@ -402,9 +412,16 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
     HF_LAUNCH(mark(0), "event record");
     HF_LAUNCH(launch_pool_keys(Kc, g, pf, kp, status, kDefaultWaitLimitNs, stream), "key pooling launch");
     HF_LAUNCH(mark(1), "event record");
-    HF_LAUNCH(launch_fwd_prologue(Q, kp, S, g, sm, idx, smma, prounds, counters, status, kDefaultWaitLimitNs, stream),
+    // the prologue converts S into the state operand unless the workspace already
+    // holds it (HF_FWD_STATE_PREPARED: written by the absorb that produced S)
+    HF_LAUNCH(launch_fwd_prologue(Q, kp, prepared ? nullptr : S, g, sm, idx, smma, prounds, counters, status,
+                                  kDefaultWaitLimitNs, stream),
               "prologue launch");
     HF_LAUNCH(mark(2), "event record");
+    // only the attention kernel reads the state (operand and z): it may wait for
+    // the absorb that the prologue did not need to wait for
+    if (state_ready)
+        HF_LAUNCH((int)cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(state_ready), 0), "state-ready event wait");
     HF_LAUNCH(launch_attn(Q, Kc, Vc, g, sm, idx, smma, z, nullptr, O, prounds, partial, counters, status,
                           kDefaultWaitLimitNs, stream),
               "hybrid attention launch");
@@ -419,10 +436,10 @@ extern "C" {
 hf_status hf_hybrid_forward_ex(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
                                int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S,
                                const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags,
-                               void* const* events)
+                               void* const* events, void* state_ready)
 {
     return forward_impl(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, flags, events,
-                        true);
+                        state_ready, true);
 }
 
 hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
@@ -431,7 +448,7 @@ hf_status hf_hybrid_forward_profiled(const hf_config* cfg, const uint16_t* Q, co
                                      void* const* events)
 {
     return hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u,
-                                events);
+                                events, nullptr);
 }
 
 hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
@@ -439,7 +456,7 @@ hf_status hf_hybrid_forward(const hf_config* cfg, const uint16_t* Q, const uint1
                             const float* z, uint16_t* O, int32_t* idx_out, void* ws, void* stream)
 {
     return hf_hybrid_forward_ex(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u,
-                                nullptr);
+                                nullptr, nullptr);
 }
 
 hf_status hf_rope_relative(const hf_config* cfg, const uint16_t* src, uint16_t* dst, int64_t head_stride,

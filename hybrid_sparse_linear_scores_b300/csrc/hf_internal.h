@@ -74,8 +74,8 @@ struct WsLayout {
     size_t counters; // uint32 [BH * pairs per head][2]: parts of a split pair that arrived (zero between calls)
     size_t qp;       // fp32 [BH][nQB][d] (hf_block_scores)
     size_t kp;       // fp32 [BH][W slots][d/4][bpf][4]: pooled keys of every ring slot (kept between calls)
-    size_t idx;      // int32 [BH][nQB][K_max]
-    size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout)
+    size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout; kept between calls)
+    size_t idx;      // int32 [BH][nQB][K_max] (the only region whose size follows topk)
     size_t prounds;  // int32 [BH * pairs per head]: rounds of each tile pair's slab stream
     size_t total_compact;   // end of the above: the attention runs without splitting pairs
     size_t partial;  // fp32 [kAttnMaxGrid][2][2][128][d + 4]: partial results of split pairs
@@ -123,7 +123,8 @@ int launch_rope(const RopeParams& p, void* stream);
 int launch_linear_read(const uint16_t* Q, const float* S, const float* z, const Geom& g, float* O, int accumulate,
                        void* stream);
 int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int64_t head_stride, const Geom& g,
-                  float* S, float* z, uint32_t* status, uint64_t wait_limit_ns, void* stream);
+                  float* S, float* z, uint16_t* smma, bool share_sms, uint32_t* status, uint64_t wait_limit_ns,
+                  void* stream);
 int launch_state_reset(float* S, float* z, const Geom& g, void* stream);
 int launch_selftest_wait(uint32_t* status, uint64_t limit_ns, void* stream);
 
@@ -133,7 +134,7 @@ int launch_selftest_wait(uint32_t* status, uint64_t limit_ns, void* stream);
 hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc,
                        int32_t slot_stride, const int32_t* slot_map, int32_t n_win, const float* S, const float* z,
                        uint16_t* O, int32_t* idx_out, void* ws, void* stream, uint32_t flags, void* const* events,
-                       bool allow_split);
+                       void* state_ready, bool allow_split);
 size_t compact_workspace_bytes(const hf_config* cfg);
 
 // Records a printf-style message as the calling thread's hf_last_error()

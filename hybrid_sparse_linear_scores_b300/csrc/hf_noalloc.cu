@@ -77,7 +77,7 @@ hf_status hf_hybrid_forward_noalloc(const hf_config* cfg, const uint16_t* Q, con
                                   dev, cudaGetErrorString(e));
     }
     if (status_word) *status_word = ws;
-    return hf::forward_impl(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u, nullptr,
+    return hf::forward_impl(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, z, O, idx_out, ws, stream, 0u, nullptr, nullptr,
                             false);
 }
 

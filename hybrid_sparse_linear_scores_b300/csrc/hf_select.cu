@@ -394,6 +394,9 @@ __device__ __forceinline__ bool wait_staged(uint64_t* bar, const WaitCtl& wc, ui
 
 // Shared-memory layout of the two bulk-pooling kernels: up to 256 staged rows,
 // reused for the scores once they are pooled.
+// Row stride (floats) of the prologue's score rows for nkb key blocks.
+__host__ __device__ constexpr int score_stride(int nkb) { return (nkb + 31) & ~31; }
+
 template <int D, int BETA>
 struct ProCfg {
     static constexpr int NT = 256;
@@ -402,14 +405,17 @@ struct ProCfg {
     static constexpr int STAGE_BYTES = 256 * D * 2;            // query rows, then 2 key-pool batches
     static constexpr int KBUF_BYTES = 2 * KB_CH * NT * 4;
     static constexpr int REGION = STAGE_BYTES > KBUF_BYTES ? STAGE_BYTES : KBUF_BYTES;
-    static constexpr int OFF_SS = REGION;                      // fp32 [QG][HF_MAX_KEY_BLOCKS] scores
-    static constexpr int OFF_QP = OFF_SS + QG * HF_MAX_KEY_BLOCKS * 4;   // fp32 [QG][D]
+    static constexpr int OFF_QP = REGION;                      // fp32 [QG][D]
     static constexpr int OFF_BITS = OFF_QP + QG * D * 4;       // uint32 [64]: slabs of the pair
     static constexpr int OFF_HIST = OFF_BITS + 64 * 4;         // uint32 [QG][256]: radix-select histograms
     static constexpr int OFF_SEL = OFF_HIST + QG * 256 * 4;    // uint32 [2][QG]: threshold prefix, count above
     static constexpr int OFF_BAR = OFF_SEL + 2 * QG * 4;       // one mbarrier
     static constexpr int OFF_MISC = OFF_BAR + 16;              // uint32 [4]
-    static constexpr int SMEM = OFF_MISC + 16;
+    static constexpr int OFF_SS = OFF_MISC + 16;               // fp32 [QG][score_stride(nkb)] scores, last:
+    static constexpr int SMEM = OFF_SS;                        //   sized per launch by the window's blocks
+    static constexpr int SMEM_MAX = OFF_SS + QG * HF_MAX_KEY_BLOCKS * 4;
+    // bytes of one launch: the scores of a window of nkb key blocks
+    static int smem_for(int nkb) { return OFF_SS + QG * score_stride(nkb) * 4; }
 };
 
 // ---------------------------------------------------------------------------
@@ -467,7 +473,8 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
                    (uint32_t)(row_end - row_start) * D * 2, bar);
 
     // 1. this CTA's rows of the state operand, while the query rows arrive
-    {
+    // (S == nullptr: the workspace already holds the operand of the current S)
+    if (S != nullptr) {
         const int rows_per = (D + groups - 1) / groups;
         const int c_lo = min(D, pair * rows_per), c_hi = min(D, c_lo + rows_per);
         uint8_t* base = reinterpret_cast<uint8_t*>(smma) + (size_t)bh * 2 * D * D * 2;
@@ -512,6 +519,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     // longer needed), the next batch in flight while the fused multiply-add
     // chains run over the current one.
     float* ss = reinterpret_cast<float*>(smem + Cfg::OFF_SS);
+    const int sst = score_stride(g.nkb);   // score row stride (floats)
     float4* kbuf = reinterpret_cast<float4*>(smem);   // [2][KB_CH / 4][NT] channel quads
     constexpr int NB = D / Cfg::KB_CH;
     constexpr int NQ4 = Cfg::KB_CH / 4;               // channel quads per batch
@@ -565,7 +573,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
         if (have) {
 #pragma unroll
             for (int q = 0; q < QG; ++q)
-                if (q < nq) ss[q * HF_MAX_KEY_BLOCKS + kb] = acc[q] + 0.0f;
+                if (q < nq) ss[q * sst + kb] = acc[q] + 0.0f;
         }
     }
     // the pair's slab set (64 key rows of one frame per slab), filled as the
@@ -591,7 +599,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     const int nkb = g.nkb, K = g.k_eff;
     for (int i = tid; i < nq * nkb; i += Cfg::NT) {
         const int q = i / nkb, kb = i - q * nkb;
-        keys[q * HF_MAX_KEY_BLOCKS + kb] = order_key(ss[q * HF_MAX_KEY_BLOCKS + kb]);
+        keys[q * sst + kb] = order_key(ss[q * sst + kb]);
     }
     if (tid < QG) {
         selP[tid] = 0u;
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
             int bin = -1;
             if (i < nq * nkb) {
                 const int q = i / nkb, kb = i - q * nkb;
-                const uint32_t k = keys[q * HF_MAX_KEY_BLOCKS + kb];
+                const uint32_t k = keys[q * sst + kb];
                 if (shift == 24 || (k >> (shift + 8)) == (selP[q] >> (shift + 8)))
                     bin = q * 256 + (int)((k >> shift) & 255u);
             }
@@ -670,7 +678,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
         }
     };
     for (int q = warp; q < nq; q += Cfg::NT / 32)
-        select_above(keys + q * HF_MAX_KEY_BLOCKS, nkb, selP[q], K - (int)selG[q],
+        select_above(keys + q * sst, nkb, selP[q], K - (int)selG[q],
                      idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
     if (!pair_rounds) return;
 
@@ -813,10 +821,10 @@ static int launch_prologue_t(const uint16_t* Q, const float* kpc, const float* S
 {
     using Cfg = ProCfg<D, BETA>;
     auto k = fwd_prologue_kernel<D, BETA>;
-    cudaError_t e = set_smem(k, Cfg::SMEM);
+    cudaError_t e = set_smem(k, Cfg::SMEM_MAX);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + Cfg::QG - 1) / Cfg::QG;
-    k<<<(unsigned)(g.BH * groups), Cfg::NT, Cfg::SMEM, st>>>(Q, kpc, S, g, sm, idx, smma, pair_rounds, counters,
+    k<<<(unsigned)(g.BH * groups), Cfg::NT, Cfg::smem_for(g.nkb), st>>>(Q, kpc, S, g, sm, idx, smma, pair_rounds, counters,
                                                             status, wait_limit_ns);
     return (int)cudaGetLastError();
 }

@@ -71,6 +71,12 @@ class HybridAttentionLayer:
         self.rope = rope
         self.Kr = torch.zeros_like(self.Kc) if rope is not None else None
         self.Qr: torch.Tensor | None = None
+        # whether the workspace holds S as the linear read's tensor-core operand:
+        # every absorb and every forward leave it so (the zeroed workspace holds
+        # the operand of S = 0); writing S directly needs state_changed()
+        self.state_prepared = True
+        self._side: torch.cuda.Stream | None = None
+        self._ev_fork = self._ev_state = None
 
     # ---- window bookkeeping (host) ----
     def n_win(self) -> int:
@@ -98,16 +104,25 @@ class HybridAttentionLayer:
         return runs
 
     # ---- the three phases of a step ----
-    def absorb_evicted(self, stream=None) -> int:
+    def absorb_evicted(self, stream=None, share_sms: bool = False) -> int:
         """Absorb the frames the next chunk evicts, from their ring slots."""
         frames = self.frames_to_evict()
         for run in self._slot_runs(frames):
-            self.absorb_slots(run[0], len(run), stream)
+            self.absorb_slots(run[0], len(run), stream, share_sms)
         return len(frames)
 
-    def absorb_slots(self, first_slot: int, n_slots: int, stream=None):
+    def absorb_slots(self, first_slot: int, n_slots: int, stream=None, share_sms: bool = False):
+        """share_sms: the absorb runs beside other kernels (on a third of the
+        SMs, fewer tiles in flight; the state differs from the unshared absorb
+        only in the order of one fp32 reduction)."""
         hb.hf_absorb_evicted_strided(self.cfg, self.S, self.z, self.Kc[:, first_slot], self.Vc[:, first_slot],
-                                     n_slots * self.nf, self.R * self.ss, self.ws, stream)
+                                     n_slots * self.nf, self.R * self.ss, self.ws, stream,
+                                     hb.HF_ABSORB_SHARE_SMS if share_sms else 0)
+        self.state_prepared = True
+
+    def state_changed(self):
+        """Call after writing S or z directly: the next forward converts S again."""
+        self.state_prepared = False
 
     def chunk_slots(self) -> list[int]:
         """Ring slots of the next chunk's frames."""
@@ -137,19 +152,26 @@ class HybridAttentionLayer:
         else:
             self.pooled.difference_update(slots)
 
+    def _state_flags(self) -> int:
+        return hb.HF_FWD_STATE_PREPARED if self.state_prepared else 0
+
     def forward(self, Q: torch.Tensor, O: torch.Tensor, idx_out: torch.Tensor | None = None, stream=None,
-                events=None):
+                events=None, state_ready=None):
         """Q, O: [BH, C*N_f, d] bf16.  idx_out: optional int32 [BH, nQB, K_eff].
         Uses the cached key pools when every window slot is in the cache;
-        otherwise pools the whole window (which fills the cache)."""
+        otherwise pools the whole window (which fills the cache).
+        state_ready: optional torch.cuda.Event (recorded after the absorb that
+        produced the state, on another stream) that the attention waits for."""
         sm = self.slot_map()
         if self.rope is not None:
-            self._forward_rope(Q, O, idx_out, stream, events)
+            self._forward_rope(Q, O, idx_out, stream, events, state_ready)
             return
         cached = all(sl in self.pooled for sl in sm)
+        flags = (hb.HF_FWD_CACHED_KEYS if cached else 0) | self._state_flags()
         hb.hf_hybrid_forward_ex(self.cfg, Q, self.Kc, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O, idx_out,
-                                self.ws, hb.HF_FWD_CACHED_KEYS if cached else 0, events, stream)
+                                self.ws, flags, events, stream, state_ready)
         self.pooled.update(sm)
+        self.state_prepared = True
 
     def rope_offsets(self) -> tuple[list[int], list[int], int]:
         """(key offsets of the window's frames in logical order, query offsets
@@ -158,7 +180,7 @@ class HybridAttentionLayer:
         bound = self.rope.max_offset if self.rope.max_offset is not None else self.window - 1
         return list(range(n)), list(range(n - self.C, n)), bound
 
-    def _forward_rope(self, Q, O, idx_out, stream, events):
+    def _forward_rope(self, Q, O, idx_out, stream, events, state_ready=None):
         """Rotate the window's keys (ring -> rotated copy) and the chunk's
         queries by their window-relative offsets, pool the rotated window's key
         blocks (every frame's offset moved with the window), then the forward
@@ -175,13 +197,35 @@ class HybridAttentionLayer:
                             r.base, stream)
         hb.hf_pool_keys(self.cfg, self.Kr, self.ss, sm, self.ws, stream)
         hb.hf_hybrid_forward_ex(self.cfg, self.Qr, self.Kr, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O,
-                                idx_out, self.ws, hb.HF_FWD_CACHED_KEYS, events, stream)
+                                idx_out, self.ws, hb.HF_FWD_CACHED_KEYS | self._state_flags(), events, stream,
+                                state_ready)
         self.pooled.clear()   # the cache holds this step's rotated pools
+        self.state_prepared = True
+
+    def can_overlap_absorb(self) -> bool:
+        """The absorb of the evicted frames may run beside the next chunk's ring
+        write, key pooling and selection when the chunk's slots are not the
+        evicted ones (spare slots) and no RoPE rewrites the window's keys."""
+        return self.rope is None and self.R >= self.window + self.C
 
     def step(self, Q, K_new, V_new, O, idx_out=None, stream=None):
-        self.absorb_evicted(stream)
-        self.write_chunk(K_new, V_new, stream)
-        self.forward(Q, O, idx_out, stream)
+        if not self.can_overlap_absorb():
+            self.absorb_evicted(stream)
+            self.write_chunk(K_new, V_new, stream)
+            self.forward(Q, O, idx_out, stream)
+            return
+        # the absorb on a side stream; ring write, key pooling and the prologue
+        # on `stream`; the attention (the only reader of the state) waits for it
+        main = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self._side is None:
+            self._side = torch.cuda.Stream(self.device)
+            self._ev_fork, self._ev_state = torch.cuda.Event(), torch.cuda.Event()
+        self._ev_fork.record(main)
+        self._side.wait_event(self._ev_fork)
+        self.absorb_evicted(self._side, share_sms=True)
+        self._ev_state.record(self._side)
+        self.write_chunk(K_new, V_new, main)
+        self.forward(Q, O, idx_out, main, state_ready=self._ev_state)
 
     # ---- checkpoint / resume ----
     def state_dict(self) -> dict:
@@ -195,6 +239,7 @@ class HybridAttentionLayer:
         self.S.copy_(sd["S"])
         self.z.copy_(sd["z"])
         self.frames = int(sd["frames"])
+        self.state_changed()
         self.invalidate_key_cache()   # the next forward re-pools the window
 
     def check_device_status(self, stream=None):

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define HF_ABI_VERSION 2
+#define HF_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define HF_API __attribute__((visibility("default")))
@@ -111,8 +111,10 @@ HF_API const char *hf_last_error(void);
  * tile pairs it splits between CTAs follow; every forward resets them before
  * its attention kernel runs, so a call that gave up part-way (a device
  * error) leaves nothing behind that changes a later call.  The workspace
- * also holds the pooled-key cache of the layer's ring (see hf_pool_keys):
- * one workspace per ring. */
+ * also holds the pooled-key cache of the layer's ring (see hf_pool_keys) and
+ * the state as the linear read's tensor-core operand (see
+ * HF_FWD_STATE_PREPARED), at offsets that do not depend on topk: one
+ * workspace per ring and state. */
 HF_API hf_status hf_workspace_size(const hf_config *cfg, size_t *bytes /* host */);
 
 /* S = 0, z = 0 (the empty state). */
@@ -123,20 +125,30 @@ HF_API hf_status hf_state_reset(const hf_config *cfg, float *S, float *z, void *
  *   S += sum_t phi(K_ev[t]) V_ev[t]^T,  z += sum_t phi(K_ev[t])
  * for every (batch, head).  K_ev, V_ev: bf16 [b, H, n_ev_tokens, d].
  * n_ev_tokens = 0 is a no-op.  tcgen05 GEMM with fp32 accumulation; phi(k)
- * enters the MMA as a bf16 hi + lo pair, so S carries ~fp32 accuracy. */
+ * enters the MMA as a bf16 hi + lo pair, so S carries ~fp32 accuracy.  The
+ * new S is also written to the workspace as the linear read's tensor-core
+ * operand (see HF_FWD_STATE_PREPARED). */
 HF_API hf_status hf_absorb_evicted(const hf_config *cfg, float *S, float *z,
                             const uint16_t *K_ev, const uint16_t *V_ev,
                             int32_t n_ev_tokens, void *ws, void *stream);
+
+/* Flag of hf_absorb_evicted_strided. */
+#define HF_ABSORB_SHARE_SMS 1u
 
 /* The same as hf_absorb_evicted, for evicted tokens that are not packed per
  * head: token t of head h is the row at K_ev + (h * head_stride_tokens + t) * d
  * (and likewise for V_ev), with head_stride_tokens >= n_ev_tokens.  This
  * absorbs frames straight out of the key/value ring (frames contiguous in
- * their slots, slot_stride = N_f) without a copy. */
+ * their slots, slot_stride = N_f) without a copy.  flags: 0, or
+ * HF_ABSORB_SHARE_SMS when the absorb runs beside other kernels (the next
+ * chunk's key pooling and the forward's prologue, on another stream): it then
+ * keeps fewer tiles in flight on a third of the SMs, so that those kernels fit
+ * beside it.  The state then differs from the other mode's only in the order
+ * of one fp32 reduction (a few ulps); each mode is deterministic. */
 HF_API hf_status hf_absorb_evicted_strided(const hf_config *cfg, float *S, float *z,
                                            const uint16_t *K_ev, const uint16_t *V_ev,
                                            int32_t n_ev_tokens, int64_t head_stride_tokens,
-                                           void *ws, void *stream);
+                                           void *ws, void *stream, uint32_t flags);
 
 /* Block importance scores (English technical summary, section 2.A.2):
  *   scores[b,h,qb,kb] = <mean(Q block qb), mean(K block kb)>  (float32)
@@ -241,20 +253,31 @@ HF_API hf_status hf_rope_relative(const hf_config *cfg, const uint16_t *src, uin
                                   (every slot of the window pooled by hf_pool_keys,
                                   or by an earlier forward, since it was last written);
                                   only the chunk's queries are pooled */
+#define HF_FWD_STATE_PREPARED 2u /* the workspace already holds the state as the
+                                  linear read's tensor-core operand: S has not
+                                  changed since the last hf_absorb_evicted(_strided)
+                                  or forward with this workspace (a fresh, zeroed
+                                  workspace holds the operand of S = 0); the forward
+                                  then does not read S (may be NULL) */
 
 /* Number of timing points of hf_hybrid_forward_ex / _profiled. */
 #define HF_FWD_EVENTS 4
 
-/* hf_hybrid_forward with options: `flags` (HF_FWD_CACHED_KEYS or 0) and
- * per-kernel timing, `events` as in hf_hybrid_forward_profiled (may be NULL).
- * Without HF_FWD_CACHED_KEYS every call pools the keys of the whole window
- * (and leaves them in the cache). */
+/* hf_hybrid_forward with options: `flags` (HF_FWD_CACHED_KEYS,
+ * HF_FWD_STATE_PREPARED, or 0), per-kernel timing, `events` as in
+ * hf_hybrid_forward_profiled (may be NULL), and `state_ready` (a cudaEvent_t,
+ * or NULL): the attention kernel, the only one that reads the state (its
+ * operand and z), waits for it on `stream`, so the key pooling and the
+ * prologue (selection) may run while an absorb on another stream is still
+ * producing the state.  Without HF_FWD_CACHED_KEYS every call pools the keys
+ * of the whole window (and leaves them in the cache). */
 HF_API hf_status hf_hybrid_forward_ex(const hf_config *cfg, const uint16_t *Q, const uint16_t *Kc,
                                       const uint16_t *Vc, int32_t slot_stride,
                                       const int32_t *slot_map /* host */, int32_t n_win,
                                       const float *S, const float *z, uint16_t *O, int32_t *idx_out,
                                       void *ws, void *stream, uint32_t flags,
-                                      void *const *events /* host, HF_FWD_EVENTS entries, or NULL */);
+                                      void *const *events /* host, HF_FWD_EVENTS entries, or NULL */,
+                                      void *state_ready /* cudaEvent_t or NULL */);
 
 /* hf_hybrid_forward with per-kernel timing.  The forward runs at most three
  * kernels: the window's key pooling (skipped with HF_FWD_CACHED_KEYS), the

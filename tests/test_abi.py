@@ -24,7 +24,7 @@ def test_library_exports_every_declared_function():
 
 def test_abi_version_and_status_strings():
     L = hb.lib()
-    assert L.hf_abi_version() == 2
+    assert L.hf_abi_version() == 3
     for code, name in hb.STATUS.items():
         assert L.hf_status_string(code).decode() == name
 

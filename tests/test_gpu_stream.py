@@ -154,3 +154,61 @@ def test_ring_write_places_frames(where, cuda_device):
         for f, sl in enumerate(slots):
             ref[:, sl, :nf] = src[:, f]
         assert torch.equal(ring.cpu().view(torch.int16), ref.view(torch.int16))
+
+
+def test_overlapped_step_matches_sequential_step(cuda_device):
+    """With spare ring slots the layer's step runs the absorb on a side stream
+    beside the ring write, key pooling and prologue (the attention waits for
+    it), on fewer SMs; indices are identical and outputs and state agree with
+    the sequential step of a layer without spare slots up to the order of the
+    absorb's cluster reduction (a few fp32 ulps of the state)."""
+    w = Workload("ovl", 1, 3, 128, 300, 3, 9, 64, seed=43, recipe="drift", topk=20, steps=7)
+    cfg = config_of(w, w.steps - 1)
+    seq = HybridAttentionLayer(cfg, cuda_device)
+    ovl = HybridAttentionLayer(cfg, cuda_device, spare_slots=w.chunk_frames)
+    assert ovl.can_overlap_absorb() and not seq.can_overlap_absorb()
+    for s in range(w.steps):
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        outs = []
+        for L in (seq, ovl):
+            O = torch.empty_like(Q)
+            idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+            L.step(Q, Kn, Vn, O, idx)
+            outs.append((O, idx))
+        torch.cuda.synchronize()
+        assert torch.equal(outs[0][1], outs[1][1]), f"step {s}"
+        a, b = outs[0][0].float(), outs[1][0].float()
+        assert float((a - b).abs().max()) <= 2.0 ** -7 * float(a.abs().max()), f"step {s}"
+        assert float((a - b).norm() / a.norm()) <= 1e-4, f"step {s}"
+    seq.check_device_status()
+    ovl.check_device_status()
+    for x, y in ((seq.S, ovl.S), (seq.z, ovl.z)):
+        assert float((x - y).norm() / x.norm()) <= 1e-6
+
+
+def test_state_operand_from_absorb_matches_prologue(cuda_device):
+    """The absorb writes the state's tensor-core operand; a forward that uses it
+    (HF_FWD_STATE_PREPARED, S not read) is bit-identical to one whose prologue
+    converts S itself."""
+    from hybrid_sparse_linear_scores_b300 import binding as hb
+    w = Workload("prep", 1, 2, 128, 300, 3, 9, 64, seed=47, recipe="drift", topk=25, steps=5)
+    cfg = config_of(w, w.steps - 1)
+    L = HybridAttentionLayer(cfg, cuda_device)
+    for s in range(w.steps - 1):
+        Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+        L.step(Q, Kn, Vn, torch.empty_like(Q))
+    s = w.steps - 1
+    Q, Kn, Vn = chunk_inputs(w, s, cuda_device)
+    L.absorb_evicted()
+    L.write_chunk(Kn, Vn)
+    outs = []
+    for flags in (hb.HF_FWD_CACHED_KEYS | hb.HF_FWD_STATE_PREPARED, hb.HF_FWD_CACHED_KEYS):
+        O = torch.empty_like(Q)
+        idx = torch.empty((w.heads_total, w.n_qb(), w.k_for(s)), dtype=torch.int32, device=cuda_device)
+        S = None if flags & hb.HF_FWD_STATE_PREPARED else L.S
+        hb.hf_hybrid_forward_ex(L.cfg, Q, L.Kc, L.Vc, L.ss, L.slot_map(), L.n_win(), S, L.z, O, idx, L.ws, flags)
+        outs.append((O, idx))
+    torch.cuda.synchronize()
+    L.check_device_status()
+    assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
