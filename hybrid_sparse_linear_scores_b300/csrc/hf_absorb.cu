@@ -475,9 +475,9 @@ int launch_absorb_t(const CUtensorMap& tk, const CUtensorMap& tv, AbsParams p, c
 template <int D, int NV, int NSX = 0>
 void pick_shape(int BH, int n_tiles, int sms, int dev, int NG, int& best_cl, int& best_score)
 {
-    // sharing the SMs (NSX > 0): at most a third of them
-    const int max_cl = NSX > 0 ? 4 : 8;
-    if (NSX > 0) sms = (sms + 2) / 3;
+    // sharing the SMs (NSX > 0): at most half of them
+    const int max_cl = NSX > 0 ? 6 : 8;
+    if (NSX > 0) sms = (sms + 1) / 2;
     for (int CL = max_cl; CL >= 1; --CL) {
         if (CL > n_tiles && CL > 1) continue;
         const long clusters = (long)BH * NG;
@@ -536,7 +536,7 @@ int launch_absorb(const uint16_t* K_ev, const uint16_t* V_ev, int32_t n_ev, int6
     const int n_tiles = (n_ev + TT - 1) / TT;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     AbsParams p{g.BH, n_ev, 1, 1, S, z, status, wait_limit_ns, smma};
-    // sharing: clusters of at most 4 CTAs on about a third of the SMs, four
+    // sharing: clusters of at most 6 CTAs on about half of the SMs, four
     // stages (about 130 KB of shared memory instead of 193), so that the key
     // pooling and the forward's prologue fit beside the absorb
     return share_sms ? launch_absorb_ns<4>(tk, tv, g, p, n_tiles, sms, dev, st)

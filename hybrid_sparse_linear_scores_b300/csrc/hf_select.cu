@@ -123,10 +123,11 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(const uint16_t* __re
 
 // ---------------------------------------------------------------------------
 // Warp top-K.  Scores are mapped to order-preserving uint32 keys (in place
-// over `s`).  The K-th largest key T is found bit by bit from the top: T is
-// the largest value with at least K keys >= T (warp-wide counts from ballots,
-// one per 32 keys).  Keys > T are all selected, keys == T are taken in
-// ascending block order until K.
+// over `s`).  The K-th largest key T: for up to 256 keys by a bitonic sort in
+// registers, beyond that bit by bit from the top (T is the largest value with
+// at least K keys >= T; warp-wide counts from ballots, one per 32 keys).
+// Keys > T are all selected, keys == T are taken in ascending block order
+// until K.
 // The winners are written in ascending block order with ballots; on_select(e)
 // is called for every winner e.
 // ---------------------------------------------------------------------------
@@ -140,6 +141,51 @@ template <typename OnSelect>
 __device__ void select_above(const uint32_t* keys, int n, uint32_t T, int remaining, int32_t* __restrict__ out,
                              OnSelect on_select);
 
+// The K-th largest of n <= 256 keys (1 <= K <= n), by one warp: a bitonic
+// sort of the keys in registers (8 per lane, element e = 32 r + lane, lanes
+// exchanged with shuffles), descending; padding keys are 0, below every key of
+// a finite score.  T = element K - 1; the number of keys above T is left to
+// the caller.
+__device__ __forceinline__ uint32_t warp_kth_largest256(const uint32_t* keys, int n, int K)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t a[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) a[r] = 32 * r + lane < n ? keys[32 * r + lane] : 0u;
+#pragma unroll
+    for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 32) {   // partner element in this lane's registers
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int p = r ^ (j >> 5);
+                    if (p > r) {
+                        const bool desc = ((32 * r) & k) == 0;   // k >= 64: the lane bits do not count
+                        const uint32_t x = a[r], y = a[p];
+                        a[r] = desc ? max(x, y) : min(x, y);
+                        a[p] = desc ? min(x, y) : max(x, y);
+                    }
+                }
+            } else {         // partner element in lane ^ j
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, a[r], j);
+                    const bool desc = ((32 * r + lane) & k) == 0;
+                    const bool lower = (lane & j) == 0;
+                    a[r] = (lower == desc) ? max(a[r], y) : min(a[r], y);
+                }
+            }
+        }
+    }
+    const int rk = (K - 1) >> 5;
+    uint32_t v = 0u;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        if (r == rk) v = a[r];
+    return __shfl_sync(0xFFFFFFFFu, v, (K - 1) & 31);
+}
+
 template <typename OnSelect>
 __device__ void warp_topk(float* s, int n, int K, int32_t* __restrict__ out, OnSelect on_select)
 {
@@ -148,23 +194,9 @@ __device__ void warp_topk(float* s, int n, int K, int32_t* __restrict__ out, OnS
     for (int e = lane; e < n; e += 32) keys[e] = order_key(s[e]);
     __syncwarp();
     uint32_t T = 0;
-    // counts of keys >= c over the warp: one ballot per 32 keys
-    if (n <= 256) {   // up to 8 keys per lane, kept in registers
-        uint32_t kr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) kr[i] = lane + 32 * i < n ? keys[lane + 32 * i] : 0u;
-        const int nfull = n >> 5, tail = n & 31;
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = T | (1u << bit);
-            int cnt = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const bool in = i < nfull || (i == nfull && lane < tail);
-                cnt += __popc(__ballot_sync(0xFFFFFFFFu, in && kr[i] >= cand));
-            }
-            if (cnt >= K) T = cand;
-        }
-    } else {
+    if (n <= 256) {
+        T = warp_kth_largest256(keys, n, K);
+    } else {   // counts of keys >= c over the warp, bit by bit: one ballot per 32 keys
         for (int bit = 31; bit >= 0; --bit) {
             const uint32_t cand = T | (1u << bit);
             int cnt = 0;
@@ -583,14 +615,15 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     for (int i = tid; i < words; i += Cfg::NT) bits[i] = 0u;
     __syncthreads();
 
-    // 4. top-K of every query block of the pair, as a radix select over the
-    // whole CTA: the K-th largest order-preserving key T is built one byte at
-    // a time (all threads histogram the current byte of the keys that match
-    // the bytes found so far, shared-memory atomics; then one warp per block
-    // finds the byte with a suffix scan), so the four levels cost four
-    // histogram passes for all blocks at once instead of a long serial
-    // search per block.  Then one warp per block writes the keys > T and the
-    // first (K - #greater) keys == T in block order, marking their slabs.
+    // 4. top-K of every query block of the pair.  The K-th largest
+    // order-preserving key T of a block: for windows of up to 256 key blocks
+    // one warp per query block sorts the block's keys in registers (bitonic);
+    // for larger windows a radix select over the whole CTA builds T one byte
+    // at a time (all threads histogram the current byte of the keys that
+    // match the bytes found so far, shared-memory atomics; then one warp per
+    // block finds the byte with a suffix scan).  Then one warp per block
+    // writes the keys > T and the first (K - #greater) keys == T in block
+    // order, marking their slabs.
     uint32_t* keys = reinterpret_cast<uint32_t*>(ss);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_HIST);
     uint32_t* selP = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_SEL);   // prefix of T
@@ -604,62 +637,6 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     if (tid < QG) {
         selP[tid] = 0u;
         selG[tid] = 0u;
-    }
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < QG * 256; i += Cfg::NT) hist[i] = 0u;
-        __syncthreads();
-        // (keys of one block crowd into a few bins, most of all at the top
-        // byte: lanes with the same bin add once, with their count)
-        for (int i0 = 0; i0 < nq * nkb; i0 += Cfg::NT) {
-            const int i = i0 + tid;
-            int bin = -1;
-            if (i < nq * nkb) {
-                const int q = i / nkb, kb = i - q * nkb;
-                const uint32_t k = keys[q * sst + kb];
-                if (shift == 24 || (k >> (shift + 8)) == (selP[q] >> (shift + 8)))
-                    bin = q * 256 + (int)((k >> shift) & 255u);
-            }
-            const uint32_t same = __match_any_sync(0xFFFFFFFFu, bin);
-            if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(same));
-        }
-        __syncthreads();
-        if (warp < nq) {
-            const int q = warp;
-            uint32_t h[8], local = 0;
-            const uint4 h0 = *reinterpret_cast<const uint4*>(hist + q * 256 + 8 * lane);
-            const uint4 h1 = *reinterpret_cast<const uint4*>(hist + q * 256 + 8 * lane + 4);
-            h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
-            h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) local += h[b];
-            uint32_t suff = local;   // keys in the bins of this lane and every higher lane
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suff, o);
-                if (lane + o < 32) suff += t;
-            }
-            const uint32_t G = selG[q];
-            uint32_t run = G + (suff - local);   // keys above this lane's bins
-            int found = -1;
-            uint32_t above_found = 0;
-#pragma unroll
-            for (int b = 7; b >= 0; --b) {
-                if (found < 0) {
-                    if (run + h[b] >= (uint32_t)K) {
-                        found = b;
-                        above_found = run;
-                    }
-                    run += h[b];
-                }
-            }
-            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, found >= 0);
-            const int top = 31 - __clz(hit);   // the highest byte value that still keeps K keys
-            if (lane == top) {
-                selP[q] |= (uint32_t)(8 * lane + found) << shift;
-                selG[q] = above_found;
-            }
-        }
-        __syncthreads();
     }
     // the block of key kb: kb / bpf by a multiply-high (exact for kb, bpf < 2^16)
     const uint32_t bpf_magic = 0xFFFFFFFFu / (uint32_t)g.bpf + 1u;
@@ -677,9 +654,80 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
             atomicOr(&bits[s0 >> 5], 1u << (s0 & 31));
         }
     };
-    for (int q = warp; q < nq; q += Cfg::NT / 32)
-        select_above(keys + q * sst, nkb, selP[q], K - (int)selG[q],
-                     idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
+    if (nkb <= 256) {
+        // one warp per query block: T by a bitonic sort of its keys in registers
+        __syncthreads();
+        for (int q = warp; q < nq; q += Cfg::NT / 32) {
+            const uint32_t* kq = keys + q * sst;
+            const uint32_t T = warp_kth_largest256(kq, nkb, K);
+            int gt = 0;
+            for (int base = 0; base < nkb; base += 32) {
+                const int e = base + lane;
+                gt += __popc(__ballot_sync(0xFFFFFFFFu, e < nkb && kq[e] > T));
+            }
+            select_above(kq, nkb, T, K - gt, idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
+        }
+    } else {
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < QG * 256; i += Cfg::NT) hist[i] = 0u;
+            __syncthreads();
+            // (keys of one block crowd into a few bins, most of all at the top
+            // byte: lanes with the same bin add once, with their count)
+            for (int i0 = 0; i0 < nq * nkb; i0 += Cfg::NT) {
+                const int i = i0 + tid;
+                int bin = -1;
+                if (i < nq * nkb) {
+                    const int q = i / nkb, kb = i - q * nkb;
+                    const uint32_t k = keys[q * sst + kb];
+                    if (shift == 24 || (k >> (shift + 8)) == (selP[q] >> (shift + 8)))
+                        bin = q * 256 + (int)((k >> shift) & 255u);
+                }
+                const uint32_t same = __match_any_sync(0xFFFFFFFFu, bin);
+                if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(same));
+            }
+            __syncthreads();
+            if (warp < nq) {
+                const int q = warp;
+                uint32_t h[8], local = 0;
+                const uint4 h0 = *reinterpret_cast<const uint4*>(hist + q * 256 + 8 * lane);
+                const uint4 h1 = *reinterpret_cast<const uint4*>(hist + q * 256 + 8 * lane + 4);
+                h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
+                h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
+    #pragma unroll
+                for (int b = 0; b < 8; ++b) local += h[b];
+                uint32_t suff = local;   // keys in the bins of this lane and every higher lane
+    #pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suff, o);
+                    if (lane + o < 32) suff += t;
+                }
+                const uint32_t G = selG[q];
+                uint32_t run = G + (suff - local);   // keys above this lane's bins
+                int found = -1;
+                uint32_t above_found = 0;
+    #pragma unroll
+                for (int b = 7; b >= 0; --b) {
+                    if (found < 0) {
+                        if (run + h[b] >= (uint32_t)K) {
+                            found = b;
+                            above_found = run;
+                        }
+                        run += h[b];
+                    }
+                }
+                const uint32_t hit = __ballot_sync(0xFFFFFFFFu, found >= 0);
+                const int top = 31 - __clz(hit);   // the highest byte value that still keeps K keys
+                if (lane == top) {
+                    selP[q] |= (uint32_t)(8 * lane + found) << shift;
+                    selG[q] = above_found;
+                }
+            }
+            __syncthreads();
+        }
+        for (int q = warp; q < nq; q += Cfg::NT / 32)
+            select_above(keys + q * sst, nkb, selP[q], K - (int)selG[q],
+                         idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
+    }
     if (!pair_rounds) return;
 
     // 5. the pair's rounds: slabs in the union of its blocks' selections

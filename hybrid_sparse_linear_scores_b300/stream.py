@@ -112,7 +112,7 @@ class HybridAttentionLayer:
         return len(frames)
 
     def absorb_slots(self, first_slot: int, n_slots: int, stream=None, share_sms: bool = False):
-        """share_sms: the absorb runs beside other kernels (on a third of the
+        """share_sms: the absorb runs beside other kernels (on about half of the
         SMs, fewer tiles in flight; the state differs from the unshared absorb
         only in the order of one fp32 reduction)."""
         hb.hf_absorb_evicted_strided(self.cfg, self.S, self.z, self.Kc[:, first_slot], self.Vc[:, first_slot],

@@ -142,7 +142,7 @@ HF_API hf_status hf_absorb_evicted(const hf_config *cfg, float *S, float *z,
  * their slots, slot_stride = N_f) without a copy.  flags: 0, or
  * HF_ABSORB_SHARE_SMS when the absorb runs beside other kernels (the next
  * chunk's key pooling and the forward's prologue, on another stream): it then
- * keeps fewer tiles in flight on a third of the SMs, so that those kernels fit
+ * keeps fewer tiles in flight on about half of the SMs, so that those kernels fit
  * beside it.  The state then differs from the other mode's only in the order
  * of one fp32 reduction (a few ulps); each mode is deterministic. */
 HF_API hf_status hf_absorb_evicted_strided(const hf_config *cfg, float *S, float *z,
