@@ -191,7 +191,8 @@ enum {
     M_TOTAL = 14,    //   total rounds of all pairs
     M_FIRSTR = 16,   // 2: first round of the part that each tile takes part in
     M_LASTR = 18,    // 2: last such round (-1: none)
-    M_OLD = 20       // 2: arrival count a tile's part found (split pairs)
+    M_OLD = 20,      // 2: arrival count a tile's part found (split pairs)
+    M_SKIPLIN = 26   // 2: this part does not finish the tile: no linear read
 };
 
 struct AttnParams {
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_init(&bar[B_LIN_FULL], 1);
                 mbar_init(&bar[B_DRAIN], 1);
+                misc[M_SKIPLIN] = misc[M_SKIPLIN + 1] = 0u;
                 fence_mbar_init();
                 // the Q tiles depend only on the pair, so they load while the list is built
                 // (the previous pair's output store has finished reading the Q region)
@@ -755,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (nblk[t] == 0) continue;
                         ok = wait_all(&bar[B_PHIQ + t], 0, SITE_ATTN_PHIQ);
                         if (!ok) break;
+                        if (*reinterpret_cast<volatile uint32_t*>(&misc[M_SKIPLIN + t]) != 0u) continue;
                         tc_fence_after();
                         const uint64_t qd = t ? q_desc1 : q_desc0;
 #pragma unroll
@@ -1013,19 +1016,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float m_own = participated ? m_use : -INFINITY;
                         const float l_own = participated ? l_tot : 0.0f;
                         if (participated) tc_fence_after();
-#pragma unroll 1
-                        for (int cb = 0; cb < D; cb += 32) {
-                            uint32_t o[32];
+                        {   // the whole row at once: one TMEM round trip
+                            uint32_t o[D / 32][32];
                             if (participated) {
-                                tmem_ld32_nw(o_col + cb, o);
+#pragma unroll
+                                for (int cq = 0; cq < D / 32; ++cq) tmem_ld32_nw(o_col + 32 * cq, o[cq]);
                                 tmem_wait_ld();
-                                reg_dep32(o);
+#pragma unroll
+                                for (int cq = 0; cq < D / 32; ++cq) reg_dep32(o[cq]);
                             } else {
 #pragma unroll
-                                for (int c = 0; c < 32; ++c) o[c] = 0u;
+                                for (int cq = 0; cq < D / 32; ++cq)
+#pragma unroll
+                                    for (int c = 0; c < 32; ++c) o[cq][c] = 0u;
                             }
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) __stcg(mine + (cb + c) * 128, __uint_as_float(o[c]));
+                            for (int cq = 0; cq < D / 32; ++cq)
+#pragma unroll
+                                for (int c = 0; c < 32; ++c)
+                                    __stcg(mine + (32 * cq + c) * 128, __uint_as_float(o[cq][c]));
                         }
                         __stcg(mine + D * 128, m_own);
                         __stcg(mine + (D + 1) * 128, l_own);
@@ -1036,7 +1045,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
                         do_out = *reinterpret_cast<volatile uint32_t*>(&misc[M_OLD + t]) == (uint32_t)(nparts - 1);
-                        if (do_out) {
+                        if (do_out && nparts == 2) {
+                            // two parts (the usual cut): the other part's whole row is
+                            // loaded at once (one memory round trip), then combined with
+                            // this part's row from TMEM in part order (CTA order), with the
+                            // same arithmetic as the general merge below
+                            __threadfence();
+                            const int oc = c0 == me ? c1 : c0;
+                            const float* src = part_col(oc);
+                            uint32_t vo[D / 32][32];
+#pragma unroll
+                            for (int cq = 0; cq < D / 32; ++cq)
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) vo[cq][k] = __float_as_uint(__ldcg(src + (32 * cq + k) * 128));
+                            const float mo = __ldcg(src + D * 128), lo = __ldcg(src + (D + 1) * 128);
+                            const float m_all = fmaxf(m_own, mo);
+                            auto scale_of = [&](float mk) { return mk == -INFINITY ? 0.0f : ex2_approx((mk - m_all) * sl2); };
+                            const float sc_me = scale_of(m_own), sc_o = scale_of(mo);
+                            const bool me_first = me < oc;
+                            l_tot = me_first ? fmaf(sc_o, lo, fmaf(sc_me, l_own, 0.0f)) : fmaf(sc_me, l_own, fmaf(sc_o, lo, 0.0f));
+#pragma unroll
+                            for (int cq = 0; cq < D / 32; ++cq) {
+                                uint32_t v[32];
+                                if (participated) {
+                                    tmem_ld32_nw(o_col + 32 * cq, v);
+                                    tmem_wait_ld();
+                                    reg_dep32(v);
+                                } else {
+#pragma unroll
+                                    for (int k = 0; k < 32; ++k) v[k] = 0u;
+                                }
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) {
+                                    const float own = __uint_as_float(v[k]), oth = __uint_as_float(vo[cq][k]);
+                                    v[k] = __float_as_uint(me_first ? fmaf(sc_o, oth, fmaf(sc_me, own, 0.0f))
+                                                                    : fmaf(sc_me, own, fmaf(sc_o, oth, 0.0f)));
+                                }
+                                tmem_st32(o_col + 32 * cq, v);
+                            }
+                            tc_fence_before();
+                            if (r == 0) p.counters[(size_t)pair * 2 + t] = 0u;   // ready for the next launch
+                        } else if (do_out) {
                             // merge in part order; this CTA's own part comes from TMEM
                             __threadfence();
                             float m_all = m_own;
@@ -1093,7 +1142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (FUSED) {
                     uint8_t* sQ = smem + Cfg::OFF_Q + t * Cfg::Q_BYTES;
                     if (ok && !do_out) {
-                        // another part finishes this pair; the MMA thread still waits for phi(Q)
+                        // another part finishes this pair: the MMA thread skips its linear read
+                        if (r == 0) misc[M_SKIPLIN + t] = 1u;
                         mbar_arrive(&bar[B_PHIQ + t]);
                     } else if (ok && (participated ||
                                       __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_Q], 0, wc, SITE_ATTN_Q)))) {
