@@ -601,22 +601,27 @@ def workload_figures(dev, flush, n):
     return out
 
 
-def pinned_h2d_rate(dev, nbytes: int = 43130880, n: int = 20):
+def pinned_h2d_rate(dev, nbytes: int = 43130880, n: int = 10, trials: int = 3):
     """GB/s of one plain copy of nbytes from pinned host memory to the device
-    (the size of a chunk's Q, K and V), CUDA events on the copying stream."""
+    (the size of a chunk's Q, K and V), CUDA events on the copying stream; the
+    best of a few trials of n copies (the host link is shared with the rest of
+    the machine)."""
     h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
     d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     st = torch.cuda.Stream(dev)
+    best = 0.0
     with torch.cuda.stream(st):
         for _ in range(3):
             d.copy_(h, non_blocking=True)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(n):
-            d.copy_(h, non_blocking=True)
-        e1.record(st)
-    torch.cuda.synchronize()
-    return nbytes * n / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        for _ in range(trials):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(n):
+                d.copy_(h, non_blocking=True)
+            e1.record(st)
+            e1.synchronize()
+            best = max(best, nbytes * n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
 
 
 def run_hf(args):
