@@ -658,9 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P V_t(r) followed by Q K^T_t(r+1) (S_t is free again once P V_t(r) has
                 // been issued: the tensor core executes in issue order).  Each tile's
                 // softmax then runs while the tensor core works on the other tile's
-                // batch.  The MMA queue holds only a few MMAs, so the thread keeps the
-                // work between batches short: round codes are read ahead, and each
-                // round's key and value stages are waited for once.
+                // batch.
                 // waits are polled by every lane and agreed on, so the warp stays converged
                 auto wait_all = [&](uint64_t* b, uint32_t parity, uint32_t site) -> bool {
                     return __all_sync(0xFFFFFFFFu, mbar_wait(b, parity, wc, site));
@@ -678,73 +676,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int last_round1 = (int)misc[M_LASTR + 1];
                 int cnt0 = 0, cnt1 = 0;
                 bool first0 = true, first1 = true;
-                int k_round = ra - 1, v_round = ra - 1;   // last round whose key / value stage was waited for
-                // m: the tile's slabs of round r (bit i = slab i), from the round code
-                // stages and phases count rounds from ra
-                auto issue_qk = [&](int r, int t, uint32_t m) -> bool {
-                    if (m == 0) return true;
-                    const int s = (r - ra) % Cfg::NR;
-                    if (r > k_round) {
-                        if (!wait_all(&bar[B_K_FULL + s], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL)) return false;
-                        k_round = r;
-                    }
-                    tc_fence_after();
-                    const uint64_t qd = t ? q_desc1 : q_desc0;
-                    // both slabs: one N = 128 operand; one slab: its 64 rows
-                    const uint64_t kd =
-                        k_desc + (uint64_t)((s * Cfg::RS_BYTES + (m == 2u ? Cfg::SLAB * 128 : 0)) >> 4);
-                    const uint32_t idesc = m == 3u ? Cfg::IDESC_QK128 : Cfg::IDESC_QK64;
-                    const uint32_t dt = tmem + 256 * t + 128;
-                    static_assert(D == 64 || Cfg::TILE_M * 128 == Cfg::CHUNK, "one chunk stride for Q and K");
-                    mma_ss_kloop_warp<D / 16, (Cfg::CHUNK >> 4)>(dt, qd, kd, idesc, 0u);
-                    mma_commit_warp(&bar[B_S_FULL + t]);
-                    return true;
-                };
-                auto issue_pv = [&](int r, int t, uint32_t m) -> bool {
-                    if (m == 0) return true;
-                    int& cnt = t ? cnt1 : cnt0;
-                    bool& first = t ? first1 : first0;
-                    if (!wait_all(&bar[B_P_FULL + t], cnt & 1, SITE_ATTN_P_FULL)) return false;
-                    ++cnt;
-                    const int s = (r - ra) % Cfg::NR;
-                    if (r > v_round) {
-                        if (!wait_all(&bar[B_V_FULL + s], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL)) return false;
-                        v_round = r;
-                    }
-                    tc_fence_after();
-                    const int n = m == 3u ? 2 : 1;
-                    const uint32_t o_tm = tmem + 256 * t;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        if (j >= n) break;
-                        const int i = (m == 2u) ? 1 : j;   // slab of the round; P columns [32j, 32j + 32)
-                        const uint64_t vd = v_desc + (uint64_t)((s * Cfg::RS_BYTES + i * Cfg::SLAB * 128) >> 4);
-                        const uint32_t at = o_tm + 128 + 32 * j;
-                        static_assert(Cfg::SLAB / 16 == 4, "four K steps per slab");
-                        mma_ts_k4_warp<(2048 >> 4)>(o_tm, at, vd, Cfg::IDESC_PV, (first && j == 0) ? 0u : 1u);
-                    }
-                    first = false;
-                    if (r == (t ? last_round1 : last_round0)) mma_commit_warp(&bar[B_O_DONE + t]);
-                    return true;
-                };
                 // One loop body for every batch, so that each batch's code exists once
                 // (the issuer then runs from a small stretch of code): for r = ra - 1
                 // .. rb - 1 and t = A, B: P V_t(r) (r >= ra), then Q K^T_t(r + 1)
                 // (r + 1 < rb).  Round codes are read one round ahead of their use.
+                // The tensor core only stays busy while MMAs are issued back to back:
+                // any other work of this thread between two MMAs idles it for that time
+                // plus a restart.  So the stages of both batches of an iteration are
+                // waited for once, before the first P, and the usual batch (both slabs
+                // of both rounds) is issued in one block without any other instruction.
                 uint32_t c_cur = 0u;
                 uint32_t c_nxt = ra < rb ? sCode[ra] : 0u;
 #pragma unroll 1
                 for (int r = ra - 1; ok && r < rb; ++r) {
                     const bool more = r + 1 < rb;
+                    const int sv = (r - ra) % Cfg::NR;       // value stage of r (r >= ra)
+                    const int sk = (r + 1 - ra) % Cfg::NR;   // key stage of r + 1
+                    if (r >= ra) ok = wait_all(&bar[B_V_FULL + sv], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL);
+                    if (ok && more) ok = wait_all(&bar[B_K_FULL + sk], ((r + 1 - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL);
 #pragma unroll 1
                     for (int t = 0; t < 2 && ok; ++t) {
-                        if (r >= ra) {
-                            ok = issue_pv(r, t, tile_bits(c_cur, t));
-                            if (ok && t == 1) mma_commit_warp(&bar[B_V_EMPTY + (r - ra) % Cfg::NR]);
+                        const uint32_t m_pv = r >= ra ? tile_bits(c_cur, t) : 0u;
+                        const uint32_t m_qk = more ? tile_bits(c_nxt, t) : 0u;
+                        int& cnt = t ? cnt1 : cnt0;
+                        bool& first = t ? first1 : first0;
+                        const int last_round = t ? last_round1 : last_round0;
+                        if (m_pv != 0u) {
+                            ok = wait_all(&bar[B_P_FULL + t], cnt & 1, SITE_ATTN_P_FULL);
+                            ++cnt;
+                            if (!ok) break;
                         }
-                        if (ok && more) {
-                            ok = issue_qk(r + 1, t, tile_bits(c_nxt, t));
-                            if (ok && t == 1) mma_commit_warp(&bar[B_K_EMPTY + (r + 1 - ra) % Cfg::NR]);
+                        tc_fence_after();
+                        const uint32_t o_tm = tmem + 256 * t;
+                        const uint64_t qd = t ? q_desc1 : q_desc0;
+                        bool done = false;
+                        if constexpr (D == 128) {
+                            if (m_pv == 3u && m_qk == 3u && r != last_round) {
+                                const uint64_t vd0 = v_desc + (uint64_t)((sv * Cfg::RS_BYTES) >> 4);
+                                const uint64_t kd = k_desc + (uint64_t)((sk * Cfg::RS_BYTES) >> 4);
+                                static_assert(Cfg::SLAB / 16 == 4, "four K steps per slab");
+                                mma_attn_batch_warp<(2048 >> 4), (Cfg::CHUNK >> 4)>(
+                                    o_tm, o_tm + 128, vd0, vd0 + (uint64_t)((Cfg::SLAB * 128) >> 4), Cfg::IDESC_PV,
+                                    first ? 0u : 1u, o_tm + 128, qd, kd, Cfg::IDESC_QK128, &bar[B_V_EMPTY + sv],
+                                    &bar[B_S_FULL + t], &bar[B_K_EMPTY + sk], t == 1 ? 1u : 0u);
+                                first = false;
+                                done = true;
+                            }
+                        }
+                        if (!done) {
+                            if (m_pv != 0u) {
+                                const int n = m_pv == 3u ? 2 : 1;
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    if (j >= n) break;
+                                    const int i = (m_pv == 2u) ? 1 : j;   // slab of the round; P columns [32j, 32j + 32)
+                                    const uint64_t vd =
+                                        v_desc + (uint64_t)((sv * Cfg::RS_BYTES + i * Cfg::SLAB * 128) >> 4);
+                                    static_assert(Cfg::SLAB / 16 == 4, "four K steps per slab");
+                                    mma_ts_k4_warp<(2048 >> 4)>(o_tm, o_tm + 128 + 32 * j, vd, Cfg::IDESC_PV,
+                                                                (first && j == 0) ? 0u : 1u);
+                                }
+                                first = false;
+                                if (r == last_round) mma_commit_warp(&bar[B_O_DONE + t]);
+                            }
+                            if (t == 1 && r >= ra) mma_commit_warp(&bar[B_V_EMPTY + sv]);
+                            if (m_qk != 0u) {
+                                // both slabs: one N = 128 operand; one slab: its 64 rows
+                                const uint64_t kd =
+                                    k_desc + (uint64_t)((sk * Cfg::RS_BYTES + (m_qk == 2u ? Cfg::SLAB * 128 : 0)) >> 4);
+                                const uint32_t idesc = m_qk == 3u ? Cfg::IDESC_QK128 : Cfg::IDESC_QK64;
+                                static_assert(D == 64 || Cfg::TILE_M * 128 == Cfg::CHUNK, "one chunk stride for Q and K");
+                                mma_ss_kloop_warp<D / 16, (Cfg::CHUNK >> 4)>(o_tm + 128, qd, kd, idesc, 0u);
+                                mma_commit_warp(&bar[B_S_FULL + t]);
+                            }
+                            if (t == 1 && more) mma_commit_warp(&bar[B_K_EMPTY + sk]);
                         }
                     }
                     c_cur = c_nxt;

@@ -288,6 +288,68 @@ __device__ __forceinline__ void mma_ts_k4_warp(uint32_t d, uint32_t a_tmem, uint
         : "memory");
 }
 
+// One full attention batch of a tile in one block, issued by one elected lane
+// of a converged warp, with no other instruction of the thread between the
+// MMAs: P V over two slabs (A = P from tensor memory, 8 columns per K step,
+// the second slab 32 columns on; B = the two value slabs vd0 / vd1, K steps
+// STEP units apart; the first MMA accumulates iff `acc`), then Q K^T into
+// `s` (A = q, B = k, eight K
+// steps: 2 units apart within a 128-byte chunk, CH units between chunks; the
+// first overwrites), and an arrival on `bar_s`.  With `rel`, arrivals on
+// `bar_v` once the P V MMAs complete and on `bar_k` once the Q K^T MMAs do.
+template <int STEP, int CH>
+__device__ __forceinline__ void mma_attn_batch_warp(uint32_t o, uint32_t p_tmem, uint64_t vd0, uint64_t vd1,
+                                                    uint32_t idesc_pv, uint32_t acc, uint32_t s, uint64_t q,
+                                                    uint64_t k, uint32_t idesc_qk, uint64_t* bar_v, uint64_t* bar_s,
+                                                    uint64_t* bar_k, uint32_t rel)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p, t, z, w;\n\t.reg .b64 ra, rb;\n\t.reg .b32 ta;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 t, %13, 0;\n\tsetp.ne.b32 z, %13, 1;\n\t"
+        "setp.ne.and.b32 w, %21, 0, e;\n\t"
+        // P V, first value slab
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+        "add.u32 ta, %1, 8;\n\tadd.s64 rb, %2, %14;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        "add.u32 ta, %1, 16;\n\tadd.s64 rb, %2, %15;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        "add.u32 ta, %1, 24;\n\tadd.s64 rb, %2, %16;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        // P V, second value slab
+        "add.u32 ta, %1, 32;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], %3, %4, t;\n\t"
+        "add.u32 ta, %1, 40;\n\tadd.s64 rb, %3, %14;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        "add.u32 ta, %1, 48;\n\tadd.s64 rb, %3, %15;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        "add.u32 ta, %1, 56;\n\tadd.s64 rb, %3, %16;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %4, t;\n\t"
+        "@w tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t"
+        // Q K^T
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], %7, %8, %9, z;\n\t"
+        "add.s64 ra, %7, 2;\n\tadd.s64 rb, %8, 2;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, 4;\n\tadd.s64 rb, %8, 4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, 6;\n\tadd.s64 rb, %8, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, %17;\n\tadd.s64 rb, %8, %17;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, %18;\n\tadd.s64 rb, %8, %18;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, %19;\n\tadd.s64 rb, %8, %19;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "add.s64 ra, %7, %20;\n\tadd.s64 rb, %8, %20;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%6], ra, rb, %9, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
+        "@w tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}"
+        ::"r"(o), "r"(p_tmem), "l"(vd0), "l"(vd1), "r"(idesc_pv), "r"(acc), "r"(s), "l"(q), "l"(k), "r"(idesc_qk),
+          "r"(smem_u32(bar_v)), "r"(smem_u32(bar_s)), "r"(smem_u32(bar_k)), "r"(1u), "n"(STEP), "n"(2 * STEP),
+          "n"(3 * STEP), "n"(CH), "n"(CH + 2), "n"(CH + 4), "n"(CH + 6), "r"(rel)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint64_t* bar)
 {
     asm volatile(
