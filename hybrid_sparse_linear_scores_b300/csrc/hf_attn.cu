@@ -1157,38 +1157,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         // phi(q) (bf16, in place over Q) and the linear-read denominator (z
                         // of the head from shared memory, four independent denominator
-                        // chains), two 16-byte chunks of the row per step.  This code runs
-                        // once per pair: kept as a small loop rather than unrolled over the
-                        // row, it is fetched once instead of as a long straight run of
-                        // instructions that all the group's warps wait for.
+                        // chains), one 64-column chunk of the row per step.  Each step
+                        // issues all its shared-memory loads (the row's eight 16-byte
+                        // pieces and the chunk's 64 values of z) before using any: while
+                        // the other tile's Q K^T keeps shared memory busy, every access
+                        // waits long, and one round trip per chunk costs far less than one
+                        // per piece.
                         const float4* zh = reinterpret_cast<const float4*>(smem + Cfg::OFF_Z);
                         float dn[4] = {g.eps, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-                        for (int k0 = 0; k0 < Cfg::DCH * 8; k0 += 2) {
-                            uint4 qv[2];
-                            uint8_t* qp2[2];
+                        for (int h = 0; h < Cfg::DCH; ++h) {
+                            uint8_t* rowp = sQ + h * (Cfg::TILE_M * 128) + r * 128;
+                            uint4 qv[8];
+                            float4 zv[16];
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int k = k0 + u;
-                                qp2[u] = sQ + (k >> 3) * (Cfg::TILE_M * 128) + r * 128 + ((((k & 7) ^ (r & 7)) & 7) << 4);
-                                qv[u] = *reinterpret_cast<const uint4*>(qp2[u]);
-                            }
+                            for (int j = 0; j < 8; ++j)
+                                qv[j] = *reinterpret_cast<const uint4*>(rowp + (((j ^ (r & 7)) & 7) << 4));
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int k = k0 + u;
-                                const float4 za = zh[2 * k], zb = zh[2 * k + 1];
-                                const float zc[8] = {za.x, za.y, za.z, za.w, zb.x, zb.y, zb.z, zb.w};
-                                uint32_t w4[4] = {qv[u].x, qv[u].y, qv[u].z, qv[u].w};
+                            for (int j = 0; j < 16; ++j) zv[j] = zh[16 * h + j];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float zc[8] = {zv[2 * j].x,     zv[2 * j].y,     zv[2 * j].z,     zv[2 * j].w,
+                                                     zv[2 * j + 1].x, zv[2 * j + 1].y, zv[2 * j + 1].z, zv[2 * j + 1].w};
+                                uint32_t w4[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
 #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     float a = bf16_lo(w4[i]), bq = bf16_hi(w4[i]);
-                                    a = a > 0.0f ? a + 1.0f : __expf(a);
-                                    bq = bq > 0.0f ? bq + 1.0f : __expf(bq);
+                                    a = phi_elu1(a);
+                                    bq = phi_elu1(bq);
                                     w4[i] = pack_bf16(a, bq);
                                     dn[i] = fmaf(bf16_lo(w4[i]), zc[2 * i], dn[i]);
                                     dn[i] = fmaf(bf16_hi(w4[i]), zc[2 * i + 1], dn[i]);
                                 }
-                                *reinterpret_cast<uint4*>(qp2[u]) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                                *reinterpret_cast<uint4*>(rowp + (((j ^ (r & 7)) & 7) << 4)) =
+                                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
                             }
                         }
                         const float den = (dn[0] + dn[1]) + (dn[2] + dn[3]);

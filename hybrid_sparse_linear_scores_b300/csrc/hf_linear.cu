@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(256) linear_read_kernel(const uint16_t* __rest
             const uint16_t* q = Q + ((size_t)bh * nq + row) * D;
             for (int c = part; c < D; c += TPR) {
                 const float x = __uint_as_float((uint32_t)q[c] << 16);
-                sphi[rl * D + c] = x > 0.0f ? x + 1.0f : __expf(x);
+                sphi[rl * D + c] = phi_elu1(x);
             }
         }
         __syncthreads();

@@ -581,4 +581,12 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// phi(x) = elu(x) + 1 = x + 1 for x > 0, e^x otherwise; e^x as 2^(x log2 e)
+// on the special-function unit (ex2.approx), which is several times cheaper
+// here than the __expf intrinsic.
+__device__ __forceinline__ float phi_elu1(float x)
+{
+    return x > 0.0f ? x + 1.0f : ex2_approx(x * 1.4426950408889634f);
+}
+
 }  // namespace hf
