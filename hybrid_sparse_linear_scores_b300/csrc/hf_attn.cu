@@ -165,10 +165,9 @@ struct AttnCfg {
 // barrier slots
 enum {
     B_Q = 0,
-    B_K_FULL = 1,      // 4 (NR)
+    B_IT_FULL = 1,     // 4 (NR): the key stage of round r + 1 and the value stage of r have landed
     B_K_EMPTY = 5,     // 4
-    B_V_FULL = 9,      // 4
-    B_V_EMPTY = 13,    // 4
+    B_V_EMPTY = 13,    // 4 (slots 9..12 unused)
     B_S_FULL = 17,     // 2 (per tile)
     B_P_FULL = 19,     // 2
     B_O_DONE = 21,     // 2
@@ -256,35 +255,60 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 }
 
 // One ring of round stages (keys or values): loads the slabs of every round
-// of the stream, in order, each into the stage of its round.  Returns the
-// number of rounds issued; *ok = false if a wait gave up.
+// of the stream, in order, each into the stage of its round.  The issuer's
+// iteration i (r = ra - 1 + i, i = 0 .. rb - ra) needs the key stage of round
+// r + 1 and the value stage of round r; one barrier per iteration covers both
+// (count 2: one arrival per ring, with its bytes), so that the issuer waits
+// once per iteration.  The key ring (shift 0) loads round ra + i for
+// iteration i, the value ring (shift 1) round ra + i - 1; the iteration with
+// no round of a ring gets that ring's arrival without bytes.  Before either
+// ring arrives for iteration i >= NR, the issuer has released the key stage
+// it used in iteration i - NR (it does so in every iteration but the last):
+// the barrier's phase of iteration i - NR has then been waited for, so no
+// arrival can land in an earlier phase and the issuer never finds the barrier
+// a phase ahead.  Returns the number of iterations the ring arrived on;
+// *ok = false if a wait gave up.
 template <int D, int BETA>
-__device__ __forceinline__ int produce_ring(const CUtensorMap* tm, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                            const uint32_t* list, int n_list, int ra, int rb, int bh,
-                                            const AttnParams& p, const WaitCtl& wc, uint32_t site, bool& ok)
+__device__ __forceinline__ int produce_ring(const CUtensorMap* tm, uint8_t* ring, uint64_t* it_full, uint64_t* empty,
+                                            uint64_t* k_empty, const uint32_t* list, int n_list, int ra, int rb,
+                                            int bh, int shift, const AttnParams& p, const WaitCtl& wc, uint32_t site,
+                                            bool& ok)
 {
     using Cfg = AttnCfg<D, BETA>;
-    int lr = 0;   // rounds are numbered from ra for the stages and phases
-    for (; lr < rb - ra; ++lr) {
+    const int n_it = rb - ra + 1;
+    int i = 0;
+    for (; i < n_it; ++i) {
+        const int lr = i - shift;   // round of this ring, counted from ra
+        const bool load = lr >= 0 && lr < rb - ra;
+        if (i >= Cfg::NR && !mbar_wait(&k_empty[(i - Cfg::NR) % Cfg::NR], ((i - Cfg::NR) / Cfg::NR) & 1, wc, site)) {
+            ok = false;
+            break;
+        }
+        if (!load) {
+            mbar_arrive(&it_full[i % Cfg::NR]);
+            continue;
+        }
         const int r = ra + lr;
         const int s = lr % Cfg::NR;
-        if (lr >= Cfg::NR && !mbar_wait(&empty[s], ((lr / Cfg::NR) - 1) & 1, wc, site)) {
+        // the stage's previous round was released (for the key ring: just waited for)
+        if (shift != 0 && lr >= Cfg::NR && !mbar_wait(&empty[s], ((lr / Cfg::NR) - 1) & 1, wc, site)) {
             ok = false;
             break;
         }
         const int nq = min(2, n_list - 2 * r);
         uint8_t* st = ring + s * Cfg::RS_BYTES;
-        mbar_arrive_expect_tx(&full[s], nq * Cfg::SLAB_BYTES);
-        for (int i = 0; i < nq; ++i) {
-            const int slab = static_cast<int>(list[2 * r + i] & 0xFFFFu);
+        mbar_arrive_expect_tx(&it_full[i % Cfg::NR], nq * Cfg::SLAB_BYTES);
+        for (int q = 0; q < nq; ++q) {
+            const int slab = static_cast<int>(list[2 * r + q] & 0xFFFFu);
             const int w = slab / p.spf;
             const int k = slab - w * p.spf;
             const int plane = bh * p.g.W + p.sm.s[w];
             for (int m = 0; m < Cfg::DCH; ++m)
-                tma_load_3d(st + m * Cfg::CHUNK + i * (Cfg::SLAB * 128), tm, &full[s], 64 * m, 64 * k, plane);
+                tma_load_3d(st + m * Cfg::CHUNK + q * (Cfg::SLAB * 128), tm, &it_full[i % Cfg::NR], 64 * m, 64 * k,
+                            plane);
         }
     }
-    return lr;
+    return i;
 }
 
 template <int D, int BETA, bool FUSED>
@@ -421,9 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) {
                 mbar_init(&bar[B_Q], 1);
                 for (int s = 0; s < Cfg::NR; ++s) {
-                    mbar_init(&bar[B_K_FULL + s], 1);
+                    mbar_init(&bar[B_IT_FULL + s], 2);   // one arrival per ring producer
                     mbar_init(&bar[B_K_EMPTY + s], 1);
-                    mbar_init(&bar[B_V_FULL + s], 1);
                     mbar_init(&bar[B_V_EMPTY + s], 1);
                 }
                 for (int t = 0; t < 2; ++t) {
@@ -622,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 0 && lane == 0) {
                 // ---------- key ring, state operand (Q was issued at the pair's start) ----------
                 bool ok = true;
-                const int issued = produce_ring<D, BETA>(&tmK, sK, &bar[B_K_FULL], &bar[B_K_EMPTY], sList, n_list,
-                                                         ra, rb, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
+                const int issued = produce_ring<D, BETA>(&tmK, sK, &bar[B_IT_FULL], &bar[B_K_EMPTY], &bar[B_K_EMPTY],
+                                                         sList, n_list, ra, rb, bh, 0, p, wc, SITE_ATTN_KV_EMPTY, ok);
                 bool lin_issued = false;
                 if (FUSED && ok) {
                     // the state operands go into the key ring once every key stage is free
@@ -639,18 +662,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // drain (bounded): every load issued has landed before the pair ends
-                for (int r = max(0, issued - Cfg::NR); r < issued; ++r)
-                    drain_wait(&bar[B_K_FULL + r % Cfg::NR], (r / Cfg::NR) & 1, p.wait_limit_ns);
+                for (int i = max(0, issued - Cfg::NR); i < issued; ++i)
+                    drain_wait(&bar[B_IT_FULL + i % Cfg::NR], (i / Cfg::NR) & 1, p.wait_limit_ns);
                 drain_wait(&bar[B_Q], 0, p.wait_limit_ns);
                 if (lin_issued) drain_wait(&bar[B_LIN_FULL], 0, p.wait_limit_ns);
                 if (!ok) *wc.abort_flag = 1;
             } else if (warp == 2 && lane == 0) {
                 // ---------- value ring ----------
                 bool ok = true;
-                const int issued = produce_ring<D, BETA>(&tmV, sV, &bar[B_V_FULL], &bar[B_V_EMPTY], sList, n_list,
-                                                         ra, rb, bh, p, wc, SITE_ATTN_KV_EMPTY, ok);
-                for (int r = max(0, issued - Cfg::NR); r < issued; ++r)
-                    drain_wait(&bar[B_V_FULL + r % Cfg::NR], (r / Cfg::NR) & 1, p.wait_limit_ns);
+                const int issued = produce_ring<D, BETA>(&tmV, sV, &bar[B_IT_FULL], &bar[B_V_EMPTY], &bar[B_K_EMPTY],
+                                                         sList, n_list, ra, rb, bh, 1, p, wc, SITE_ATTN_KV_EMPTY, ok);
+                for (int i = max(0, issued - Cfg::NR); i < issued; ++i)
+                    drain_wait(&bar[B_IT_FULL + i % Cfg::NR], (i / Cfg::NR) & 1, p.wait_limit_ns);
                 if (!ok) *wc.abort_flag = 1;
             } else if (warp == 1) {
                 // ---------- MMA issuer (the whole warp, converged; one elected lane issues) ----------
@@ -692,8 +715,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool more = r + 1 < rb;
                     const int sv = (r - ra) % Cfg::NR;       // value stage of r (r >= ra)
                     const int sk = (r + 1 - ra) % Cfg::NR;   // key stage of r + 1
-                    if (r >= ra) ok = wait_all(&bar[B_V_FULL + sv], ((r - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL);
-                    if (ok && more) ok = wait_all(&bar[B_K_FULL + sk], ((r + 1 - ra) / Cfg::NR) & 1, SITE_ATTN_KV_FULL);
+                    {   // the key stage of r + 1 and the value stage of r: one barrier
+                        const int it = r + 1 - ra;
+                        ok = wait_all(&bar[B_IT_FULL + it % Cfg::NR], (it / Cfg::NR) & 1, SITE_ATTN_KV_FULL);
+                    }
 #pragma unroll 1
                     for (int t = 0; t < 2 && ok; ++t) {
                         const uint32_t m_pv = r >= ra ? tile_bits(c_cur, t) : 0u;
