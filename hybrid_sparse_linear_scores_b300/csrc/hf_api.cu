@@ -391,6 +391,15 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(w + L.idx);
     uint16_t* smma = reinterpret_cast<uint16_t*>(w + L.smma);
     uint32_t* status = reinterpret_cast<uint32_t*>(w + L.status);
+    // Cutting tile pairs between CTAs balances weighted rounds in 32-bit unit
+    // counts: at most round_weight(2, 2) per round and kPartWeight per pair.
+    // Layers too large for that (far beyond a realistic layer) run whole pairs.
+    {
+        const long per_tile = 128 / g.beta;
+        const long pairs = (long)g.BH * ((((long)g.nqb + per_tile - 1) / per_tile + 1) / 2);
+        const long max_rounds = ((long)g.n_win * ((g.nf + 63) / 64) + 1) / 2;
+        if (pairs * ((long)round_weight(2, 2) * max_rounds + (long)kPartWeight) >= (1L << 31)) allow_split = false;
+    }
     int32_t* prounds = allow_split ? reinterpret_cast<int32_t*>(w + L.prounds) : nullptr;
     float* partial = allow_split ? reinterpret_cast<float*>(w + L.partial) : nullptr;
     uint32_t* counters = allow_split ? reinterpret_cast<uint32_t*>(w + L.counters) : nullptr;

@@ -191,7 +191,10 @@ enum {
     M_FIRSTR = 16,   // 2: first round of the part that each tile takes part in
     M_LASTR = 18,    // 2: last such round (-1: none)
     M_OLD = 20,      // 2: arrival count a tile's part found (split pairs)
-    M_SKIPLIN = 26   // 2: this part does not finish the tile: no linear read
+    M_SKIPLIN = 26,  // 2: this part does not finish the tile: no linear read
+    M_WSUM = 3,      // 4: per-warp weight sums of the list's rounds
+    M_RA = 28,       // first round of this part
+    M_RB = 29        // end of this part's rounds
 };
 
 struct AttnParams {
@@ -215,11 +218,15 @@ struct AttnParams {
     uint32_t* counters;           // [total_pairs][2] parts arrived per tile; zero between launches
 };
 
-// Balancing units: each pair counts kPartUnits units ahead of its rounds, so
-// that the fixed cost of a part (list build, pipeline fill, epilogue: about
-// eight rounds' time on the realistic workload) is shared out too; round x of
-// a pair whose units start at P is unit P + kPartUnits + x.
-constexpr uint32_t kPartUnits = 8;
+// Balancing units: each round of a pair counts round_weight units (its MMA
+// work), and each pair counts kPartWeight units ahead of its rounds, so that
+// the fixed cost of a part (list build, pipeline fill, epilogue) is shared out
+// too.  The prologue writes each pair's total weight; round r of a pair whose
+// units start at P starts at unit P + kPartWeight + (weights of rounds < r).
+__device__ __forceinline__ uint32_t code_weight(uint32_t code)
+{
+    return round_weight(__popc(code & 3u), __popc((code >> 2) & 3u));
+}
 
 // CTA owning global round x when T rounds are cut into G equal shares
 // (CTA c takes rounds [c T / G, (c + 1) T / G)).
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int per = (NP + kThreads - 1) / kThreads;
         const int b0 = min(NP, tid * per), b1 = min(NP, b0 + per);
         int loc = 0;
-        for (int i = b0; i < b1; ++i) loc += p.pair_rounds[i] + (int)kPartUnits;
+        for (int i = b0; i < b1; ++i) loc += p.pair_rounds[i] + (int)kPartWeight;
         tsum[tid] = loc;
         if (tid == 0) {
             misc[M_PFIRST] = (uint32_t)NP;   // none, unless found below
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         e_c = share_start(blockIdx.x + 1, T, gridDim.x);
         uint32_t P = (uint32_t)tsum[tid];
         for (int i = b0; i < b1; ++i) {
-            const uint32_t R = (uint32_t)p.pair_rounds[i] + kPartUnits;   // units of the pair
+            const uint32_t R = (uint32_t)p.pair_rounds[i] + kPartWeight;   // units of the pair
             if (P <= s_c && s_c < P + R) {
                 misc[M_PFIRST] = (uint32_t)i;
                 misc[M_PREF] = P;
@@ -427,15 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pair = pair_first;
         uint32_t P = pref_first;
         for (;;) {
-            // this part of the pair: rounds [ra, rb) of its stream
+            // this part of the pair: the pair's units [lo, hi) (counted from its
+            // round 0); its rounds [ra, rb), the rounds that start there, follow from
+            // the rounds' weights once the slab list is built
             int ra = 0, rb = 1 << 30;
-            uint32_t R = 0;
+            uint32_t R = 0, lo = 0, hi = 0xFFFFFFFFu;
             if (split) {
-                if (pair >= p.total_pairs || P + kPartUnits >= e_c || s_c >= e_c) break;
-                R = (uint32_t)p.pair_rounds[pair];
-                const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
-                ra = (int)(max(s_c, Pr) - Pr);
-                rb = (int)(min(e_c, Pr + R) - Pr);
+                if (pair >= p.total_pairs || P + kPartWeight >= e_c || s_c >= e_c) break;
+                R = (uint32_t)p.pair_rounds[pair];    // the pair's weight
+                const uint32_t Pr = P + kPartWeight;   // unit of the pair's round 0
+                lo = max(s_c, Pr) - Pr;
+                hi = min(e_c, Pr + R) - Pr;
             } else if (pair >= p.total_pairs) {
                 break;
             }
@@ -602,9 +611,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (tid == 0) {
                     misc[M_NLIST] = base_out;
-                    if (split && (uint32_t)(base_out + 1) / 2 != R) report_error(wc, HF_DEV_ERR_CHECK, SITE_ATTN_BAD_INDEX);
                     misc[M_FIRSTR] = misc[M_FIRSTR + 1] = 0x7FFFFFFFu;
                     misc[M_LASTR] = misc[M_LASTR + 1] = 0xFFFFFFFFu;
+                    misc[M_RA] = misc[M_RB] = 0u;
                 }
                 for (int r = tid; r < (base_out + 1) / 2; r += 128) {
                     uint32_t c = 0;
@@ -619,6 +628,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sCode[r] = static_cast<uint8_t>(c);
                 }
                 bar_ctl();
+                {   // The part's rounds: round r starts at the sum of the weights of the
+                    // rounds before it; this part takes the rounds that start in [lo, hi)
+                    // (the neighbouring CTA's share starts where this one ends, so every
+                    // round has exactly one owner).  Each thread sums a run of
+                    // consecutive rounds; a scan over the runs gives every start.
+                    const int nr = (base_out + 1) / 2;
+                    const int CH = (nr + 127) / 128;
+                    const int r0 = min(nr, tid * CH), r1 = min(nr, r0 + CH);
+                    uint32_t wsum = 0;
+                    for (int r = r0; r < r1; ++r) wsum += code_weight(sCode[r]);
+                    uint32_t inc = wsum;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+                        if (lane >= o) inc += v;
+                    }
+                    if (lane == 31) misc[M_WSUM + warp] = inc;
+                    bar_ctl();
+                    uint32_t st = inc - wsum, total = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t wq = misc[M_WSUM + q];
+                        if (q < warp) st += wq;
+                        total += wq;
+                    }
+                    uint32_t n_lo = 0, n_hi = 0;
+                    for (int r = r0; r < r1; ++r) {
+                        n_lo += st < lo ? 1u : 0u;
+                        n_hi += st < hi ? 1u : 0u;
+                        st += code_weight(sCode[r]);
+                    }
+                    n_lo = __reduce_add_sync(0xFFFFFFFFu, n_lo);
+                    n_hi = __reduce_add_sync(0xFFFFFFFFu, n_hi);
+                    if (lane == 0) {
+                        atomicAdd(&misc[M_RA], n_lo);
+                        atomicAdd(&misc[M_RB], n_hi);
+                    }
+                    // the prologue's weight of the pair is the weight of this list
+                    if (tid == 0 && split && total != R) report_error(wc, HF_DEV_ERR_CHECK, SITE_ATTN_BAD_INDEX);
+                    bar_ctl();
+                    ra = (int)misc[M_RA];
+                    rb = (int)misc[M_RB];
+                }
                 // first and last round of this part that each tile takes part in
                 const int rend = min(rb, (base_out + 1) / 2);
                 for (int r = ra + tid; r < rend; r += 128) {
@@ -821,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (stop) break;
             if (split) {
-                P += R + kPartUnits;
+                P += R + kPartWeight;
                 ++pair;
             } else {
                 pair += gridDim.x;
@@ -834,15 +886,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pair = pair_first;
         uint32_t P = pref_first;
         for (;;) {
-            // this part of the pair: rounds [ra, rb) of its stream (as in warpgroup 0)
-            int ra = 0, rb = 1 << 30;
+            // this part of the pair (as in warpgroup 0, which finds its rounds)
             uint32_t R = 0;
             if (split) {
-                if (pair >= p.total_pairs || P + kPartUnits >= e_c || s_c >= e_c) break;
+                if (pair >= p.total_pairs || P + kPartWeight >= e_c || s_c >= e_c) break;
                 R = (uint32_t)p.pair_rounds[pair];
-                const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
-                ra = (int)(max(s_c, Pr) - Pr);
-                rb = (int)(min(e_c, Pr + R) - Pr);
             } else if (pair >= p.total_pairs) {
                 break;
             }
@@ -853,7 +901,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (bar_all_or(*wc.abort_flag != 0)) break;   // list and barriers ready
             const int n_list = (int)misc[M_NLIST];
             const int n_rounds = (n_list + 1) / 2;
-            rb = min(rb, n_rounds);
+            // this part's rounds [ra, rb) of the pair's stream
+            const int ra = (int)misc[M_RA];
+            const int rb = min((int)misc[M_RB], n_rounds);
             const bool participated = (int)misc[M_LASTR + t] >= 0;   // in a round of this part
             if (nblk > 0) {
                 const int quarter = warp & 3;            // TMEM lane quarter this warp may access
@@ -1028,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int G = gridDim.x;
                     // parts: the CTAs c0..c1 with a non-empty share (c0 and c1 own rounds,
                     // so their shares are never empty)
-                    const uint32_t Pr = P + kPartUnits;   // unit of the pair's round 0
+                    const uint32_t Pr = P + kPartWeight;   // unit of the pair's round 0
                     const int c0 = round_owner(Pr, T, G);
                     const int c1 = round_owner(Pr + R - 1, T, G);
                     int nparts = 0;
@@ -1303,7 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (stop) break;
             if (split) {
-                P += R + kPartUnits;
+                P += R + kPartWeight;
                 ++pair;
             } else {
                 pair += gridDim.x;

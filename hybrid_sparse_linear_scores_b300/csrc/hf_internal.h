@@ -82,6 +82,19 @@ struct WsLayout {
     size_t total;
 };
 
+// Balancing weight of one round of a tile pair's slab stream, in the units of
+// the attention kernel's equal shares per CTA: a fixed part plus the MMAs of
+// each tile that takes part in the round (4 per slab of P V, 8 of Q K^T),
+// halved.  sa, sb: slabs of the round that tile A / tile B needs (0..2).  A
+// round of both tiles costs about 1.35 times a round of one tile.
+__host__ __device__ constexpr uint32_t round_weight(int sa, int sb)
+{
+    return 15u + (sa ? 2u * (uint32_t)sa + 4u : 0u) + (sb ? 2u * (uint32_t)sb + 4u : 0u);
+}
+// Units charged to each pair part on top of its rounds (epilogue and slab
+// list, about eight rounds of both tiles).
+constexpr uint32_t kPartWeight = 248;
+
 // Largest attention grid (one CTA per SM, at most this many): the partial
 // results of split pairs are sized for it.
 constexpr int kAttnMaxGrid = 160;

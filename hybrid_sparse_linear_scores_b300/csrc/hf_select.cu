@@ -438,8 +438,8 @@ struct ProCfg {
     static constexpr int KBUF_BYTES = 2 * KB_CH * NT * 4;
     static constexpr int REGION = STAGE_BYTES > KBUF_BYTES ? STAGE_BYTES : KBUF_BYTES;
     static constexpr int OFF_QP = REGION;                      // fp32 [QG][D]
-    static constexpr int OFF_BITS = OFF_QP + QG * D * 4;       // uint32 [64]: slabs of the pair
-    static constexpr int OFF_HIST = OFF_BITS + 64 * 4;         // uint32 [QG][256]: radix-select histograms
+    static constexpr int OFF_BITS = OFF_QP + QG * D * 4;       // uint32 [2][64]: slabs of tile A / tile B
+    static constexpr int OFF_HIST = OFF_BITS + 2 * 64 * 4;     // uint32 [QG][256]: radix-select histograms
     static constexpr int OFF_SEL = OFF_HIST + QG * 256 * 4;    // uint32 [2][QG]: threshold prefix, count above
     static constexpr int OFF_BAR = OFF_SEL + 2 * QG * 4;       // one mbarrier
     static constexpr int OFF_MISC = OFF_BAR + 16;              // uint32 [4]
@@ -462,10 +462,38 @@ struct ProCfg {
 //      cache (one key block per thread, a fused multiply-add chain in
 //      ascending channel order per query block);
 //   4. top-K per query block (one warp per block);
-//   5. the pair's round count for the attention kernel's balancing: the
-//      slabs (64 key rows of one frame) in the union of its blocks'
-//      selections, halved and rounded up; and its arrival counters zeroed.
+//   5. the pair's weight for the attention kernel's balancing: the rounds of
+//      its slab stream (slabs: 64 key rows of one frame, in the union of its
+//      blocks' selections) in the attention kernel's order, each weighted by
+//      round_weight; and its arrival counters zeroed.
 // ---------------------------------------------------------------------------
+// Weight of a tile pair's slab stream in the attention kernel's order: the
+// nI2 = nI & ~1 slabs both tiles need (rounds of both tiles), then
+// mp = 2 min(nA / 2, nB / 2) slabs of each tile alone in alternating rounds of
+// two, then the rest of tile A's and of tile B's own slabs, then the odd slab
+// of both; a round is two consecutive slabs of the stream.
+__device__ uint32_t pair_weight(int nI, int nA, int nB)
+{
+    const int nI2 = nI & ~1, mp = 2 * min(nA >> 1, nB >> 1);
+    uint32_t w = (uint32_t)(nI2 / 2) * round_weight(2, 2) +
+                 (uint32_t)(mp / 2) * (round_weight(2, 0) + round_weight(0, 2));
+    // the rest, A^a B^b I^c, from an even position of the stream
+    const int a = nA - mp, c = nI & 1;
+    int b = nB - mp;
+    w += (uint32_t)(a / 2) * round_weight(2, 0);
+    if (a & 1) {   // the last slab of tile A alone shares its round with the next slab
+        if (b > 0) {
+            w += round_weight(1, 1);
+            --b;
+        } else {
+            return w + (c ? round_weight(2, 1) : round_weight(1, 0));
+        }
+    }
+    w += (uint32_t)(b / 2) * round_weight(0, 2);
+    if (b & 1) return w + (c ? round_weight(1, 2) : round_weight(0, 1));
+    return w + (c ? round_weight(1, 1) : 0u);
+}
+
 template <int D, int BETA>
 __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __restrict__ Q,
                                                            const float* __restrict__ kpc,
@@ -612,7 +640,7 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     // blocks are selected
     const int spf = (g.nf + 63) / 64;
     const int words = (g.n_win * spf + 31) / 32;
-    for (int i = tid; i < words; i += Cfg::NT) bits[i] = 0u;
+    for (int i = tid; i < 2 * 64; i += Cfg::NT) bits[i] = 0u;
     __syncthreads();
 
     // 4. top-K of every query block of the pair.  The K-th largest
@@ -640,18 +668,20 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     }
     // the block of key kb: kb / bpf by a multiply-high (exact for kb, bpf < 2^16)
     const uint32_t bpf_magic = 0xFFFFFFFFu / (uint32_t)g.bpf + 1u;
-    auto mark = [&](int kb) {
+    // (slab bits per tile: query block q belongs to tile 2 q / QG of the pair)
+    auto mark = [&](int kb, int t) {
+        uint32_t* bt = bits + 64 * t;
         const int w = (int)__umulhi((uint32_t)kb, bpf_magic), j = kb - w * g.bpf;
         if (BETA == 64) {
             const int s0 = w * spf + j;
-            atomicOr(&bits[s0 >> 5], 1u << (s0 & 31));
+            atomicOr(&bt[s0 >> 5], 1u << (s0 & 31));
         } else if (BETA == 128) {
             const int s0 = w * spf + 2 * j;
-            atomicOr(&bits[s0 >> 5], 1u << (s0 & 31));
-            if (2 * j + 1 < spf) atomicOr(&bits[(s0 + 1) >> 5], 1u << ((s0 + 1) & 31));
+            atomicOr(&bt[s0 >> 5], 1u << (s0 & 31));
+            if (2 * j + 1 < spf) atomicOr(&bt[(s0 + 1) >> 5], 1u << ((s0 + 1) & 31));
         } else {
             const int s0 = w * spf + (j >> 1);
-            atomicOr(&bits[s0 >> 5], 1u << (s0 & 31));
+            atomicOr(&bt[s0 >> 5], 1u << (s0 & 31));
         }
     };
     if (nkb <= 256) {
@@ -665,7 +695,8 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
                 const int e = base + lane;
                 gt += __popc(__ballot_sync(0xFFFFFFFFu, e < nkb && kq[e] > T));
             }
-            select_above(kq, nkb, T, K - gt, idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
+            select_above(kq, nkb, T, K - gt, idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff,
+                         [&](int kb) { mark(kb, (2 * q) / QG); });
         }
     } else {
         for (int shift = 24; shift >= 0; shift -= 8) {
@@ -726,20 +757,27 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
         }
         for (int q = warp; q < nq; q += Cfg::NT / 32)
             select_above(keys + q * sst, nkb, selP[q], K - (int)selG[q],
-                         idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, mark);
+                         idx + ((size_t)bh * g.nqb + qb0 + q) * g.k_eff, [&](int kb) { mark(kb, (2 * q) / QG); });
     }
     if (!pair_rounds) return;
 
-    // 5. the pair's rounds: slabs in the union of its blocks' selections
+    // 5. the pair's weight: its slabs by tile (both, tile A only, tile B only)
     __syncthreads();
     if (warp == 0) {
         const int lane = tid & 31;
-        int cnt = 0;
-        for (int i = lane; i < words; i += 32) cnt += __popc(bits[i]);
-        cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+        int nI = 0, nA = 0, nB = 0;
+        for (int i = lane; i < words; i += 32) {
+            const uint32_t a = bits[i], b = bits[64 + i];
+            nI += __popc(a & b);
+            nA += __popc(a & ~b);
+            nB += __popc(b & ~a);
+        }
+        nI = __reduce_add_sync(0xFFFFFFFFu, nI);
+        nA = __reduce_add_sync(0xFFFFFFFFu, nA);
+        nB = __reduce_add_sync(0xFFFFFFFFu, nB);
         if (lane == 0) {
             const size_t pr = (size_t)bh * groups + pair;
-            pair_rounds[pr] = (cnt + 1) / 2;
+            pair_rounds[pr] = (int32_t)pair_weight(nI, nA, nB);
             // the attention kernel that follows counts the parts of a split
             // pair here; a launch that gave up part-way can leave a count behind
             counters[2 * pr] = 0u;
