@@ -573,6 +573,10 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
     }
     __syncthreads();
 
+    // the key pools of the new frames come from the key pooling launched just
+    // before this kernel (a programmatic dependency: this kernel may have
+    // started while it ran)
+    griddep_wait();
     // 3. scores.  A thread's key block: its pooled channels are copied from
     // the cache into the thread's own column of a batch buffer (cp.async,
     // KB_CH channels per batch, two batches over the staged rows, which are no
@@ -799,6 +803,9 @@ __global__ void __launch_bounds__(256) pool_keys_kernel(const uint16_t* __restri
     using Cfg = ProCfg<D, BETA>;
     constexpr int QG = Cfg::QG;
     extern __shared__ __align__(128) uint8_t smem[];
+    // the forward prologue that follows may start now: it waits for this
+    // kernel's pooled keys only before its scores
+    griddep_launch_dependents();
     float* qps = reinterpret_cast<float*>(smem + Cfg::OFF_QP);
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint32_t* misc = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
@@ -910,9 +917,19 @@ static int launch_prologue_t(const uint16_t* Q, const float* kpc, const float* S
     cudaError_t e = set_smem(k, Cfg::SMEM_MAX);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + Cfg::QG - 1) / Cfg::QG;
-    k<<<(unsigned)(g.BH * groups), Cfg::NT, Cfg::smem_for(g.nkb), st>>>(Q, kpc, S, g, sm, idx, smma, pair_rounds, counters,
-                                                            status, wait_limit_ns);
-    return (int)cudaGetLastError();
+    // programmatic stream serialization: the kernel may start while the key
+    // pooling before it runs (it waits for it before its scores)
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)(g.BH * groups));
+    lc.blockDim = dim3(Cfg::NT);
+    lc.dynamicSmemBytes = (size_t)Cfg::smem_for(g.nkb);
+    lc.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return (int)cudaLaunchKernelEx(&lc, k, Q, kpc, S, g, sm, idx, smma, pair_rounds, counters, status, wait_limit_ns);
 }
 
 int launch_fwd_prologue(const uint16_t* Q, const float* kpc, const float* S, const Geom& g, const SlotMap& sm,
