@@ -92,8 +92,9 @@ __host__ __device__ constexpr uint32_t round_weight(int sa, int sb)
     return 15u + (sa ? 2u * (uint32_t)sa + 4u : 0u) + (sb ? 2u * (uint32_t)sb + 4u : 0u);
 }
 // Units charged to each pair part on top of its rounds (epilogue and slab
-// list, about eight rounds of both tiles).
-constexpr uint32_t kPartWeight = 248;
+// list: about six rounds of both tiles; 160-200 measured best, 248 and 300
+// slower by 1 and 4 us on the realistic layer).
+constexpr uint32_t kPartWeight = 192;
 
 // Largest attention grid (one CTA per SM, at most this many): the partial
 // results of split pairs are sized for it.
