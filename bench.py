@@ -669,7 +669,8 @@ def run_hf(args):
         if events is not None:
             events[2].record(stream)
         L.pool_slots(chunk_slots, stream)
-        L.forward(Q, O, idx, stream, events[3:] if events is not None else None, state_ready=ev_state)
+        L.forward(Q, O, idx, stream, events[3:] if events is not None else None, state_ready=ev_state,
+                  after_pool_keys=True)
 
     stream = torch.cuda.current_stream(dev)
     L.forward(Q, O, idx, stream)                          # fills the key-pool cache for the window

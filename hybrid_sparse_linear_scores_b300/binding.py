@@ -196,6 +196,7 @@ def hf_hybrid_forward_profiled(cfg, Q, Kc, Vc, slot_stride, slot_map, n_win, S, 
 
 HF_FWD_CACHED_KEYS = 1
 HF_FWD_STATE_PREPARED = 2
+HF_FWD_AFTER_POOL_KEYS = 4
 HF_ABSORB_SHARE_SMS = 1
 HF_FWD_EVENTS = 4
 

@@ -371,7 +371,7 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
 {
     hf_status s = check_cfg(cfg);
     if (s != HF_OK) return s;
-    if (flags & ~(uint32_t)(HF_FWD_CACHED_KEYS | HF_FWD_STATE_PREPARED))
+    if (flags & ~(uint32_t)(HF_FWD_CACHED_KEYS | HF_FWD_STATE_PREPARED | HF_FWD_AFTER_POOL_KEYS))
         return fail(HF_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     const bool prepared = (flags & HF_FWD_STATE_PREPARED) != 0;
     HF_CHECK_PTR(Q);
@@ -423,8 +423,11 @@ hf_status forward_impl(const hf_config* cfg, const uint16_t* Q, const uint16_t* 
     HF_LAUNCH(mark(1), "event record");
     // the prologue converts S into the state operand unless the workspace already
     // holds it (HF_FWD_STATE_PREPARED: written by the absorb that produced S)
+    // the prologue may start while a key pooling launched just before it runs:
+    // the one above, or (HF_FWD_AFTER_POOL_KEYS) the caller's hf_pool_keys
+    const bool after_pool = pf.n > 0 || (flags & HF_FWD_AFTER_POOL_KEYS) != 0;
     HF_LAUNCH(launch_fwd_prologue(Q, kp, prepared ? nullptr : S, g, sm, idx, smma, prounds, counters, status,
-                                  kDefaultWaitLimitNs, stream),
+                                  kDefaultWaitLimitNs, after_pool, stream),
               "prologue launch");
     HF_LAUNCH(mark(2), "event record");
     // only the attention kernel reads the state (operand and z): it may wait for

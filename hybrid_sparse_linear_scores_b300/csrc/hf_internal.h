@@ -110,10 +110,13 @@ int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream);
 // The hybrid forward's prologue in one launch: pooling of the chunk's query
 // blocks, the state as the epilogue's tensor-core operand (S -> bf16 hi/lo),
 // scores against the cached key pools, top-K and, when pair_rounds is given,
-// each tile pair's round count (and its arrival counters zeroed).
+// each tile pair's weight (and its arrival counters zeroed).  after_pool: the
+// kernel launched just before on `stream` is a key pooling, and the prologue
+// may start while it runs (it reads Q and S meanwhile, the pooled keys only
+// after waiting for it).
 int launch_fwd_prologue(const uint16_t* Q, const float* kpc, const float* S, const Geom& g, const SlotMap& sm,
                         int32_t* idx, uint16_t* smma, int32_t* pair_rounds, uint32_t* counters, uint32_t* status,
-                        uint64_t wait_limit_ns, void* stream);
+                        uint64_t wait_limit_ns, bool after_pool, void* stream);
 // Key-block pooling of ring slots pf.slot[0..pf.n) into the cache, bulk copies.
 int launch_pool_keys(const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* kpc, uint32_t* status,
                      uint64_t wait_limit_ns, void* stream);

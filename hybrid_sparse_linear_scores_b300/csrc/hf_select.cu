@@ -910,15 +910,16 @@ int launch_topk(const float* scores, const Geom& g, int32_t* idx, void* stream)
 template <int D, int BETA>
 static int launch_prologue_t(const uint16_t* Q, const float* kpc, const float* S, const Geom& g, const SlotMap& sm,
                              int32_t* idx, uint16_t* smma, int32_t* pair_rounds, uint32_t* counters,
-                             uint32_t* status, uint64_t wait_limit_ns, cudaStream_t st)
+                             uint32_t* status, uint64_t wait_limit_ns, bool after_pool, cudaStream_t st)
 {
     using Cfg = ProCfg<D, BETA>;
     auto k = fwd_prologue_kernel<D, BETA>;
     cudaError_t e = set_smem(k, Cfg::SMEM_MAX);
     if (e != cudaSuccess) return (int)e;
     const int groups = (g.nqb + Cfg::QG - 1) / Cfg::QG;
-    // programmatic stream serialization: the kernel may start while the key
-    // pooling before it runs (it waits for it before its scores)
+    // after a key pooling: programmatic stream serialization, the kernel may start
+    // while the key pooling runs (it waits for it before its scores).  Otherwise
+    // an ordinary launch: whatever ran before may have written Q or S.
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)(g.BH * groups));
     lc.blockDim = dim3(Cfg::NT);
@@ -928,20 +929,20 @@ static int launch_prologue_t(const uint16_t* Q, const float* kpc, const float* S
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    lc.numAttrs = after_pool ? 1 : 0;
     return (int)cudaLaunchKernelEx(&lc, k, Q, kpc, S, g, sm, idx, smma, pair_rounds, counters, status, wait_limit_ns);
 }
 
 int launch_fwd_prologue(const uint16_t* Q, const float* kpc, const float* S, const Geom& g, const SlotMap& sm,
                         int32_t* idx, uint16_t* smma, int32_t* pair_rounds, uint32_t* counters, uint32_t* status,
-                        uint64_t wait_limit_ns, void* stream)
+                        uint64_t wait_limit_ns, bool after_pool, void* stream)
 {
     if (pair_rounds && !counters) return (int)cudaErrorInvalidValue;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define HF_PRO_CASE(DD, BB)                                                                                   \
     if (g.d == DD && g.beta == BB)                                                                            \
         return launch_prologue_t<DD, BB>(Q, kpc, S, g, sm, idx, smma, pair_rounds, counters, status,          \
-                                         wait_limit_ns, st);
+                                         wait_limit_ns, after_pool, st);
     HF_PRO_CASE(128, 64)
     HF_PRO_CASE(128, 128)
     HF_PRO_CASE(128, 32)

@@ -156,18 +156,23 @@ class HybridAttentionLayer:
         return hb.HF_FWD_STATE_PREPARED if self.state_prepared else 0
 
     def forward(self, Q: torch.Tensor, O: torch.Tensor, idx_out: torch.Tensor | None = None, stream=None,
-                events=None, state_ready=None):
+                events=None, state_ready=None, after_pool_keys: bool = False):
         """Q, O: [BH, C*N_f, d] bf16.  idx_out: optional int32 [BH, nQB, K_eff].
         Uses the cached key pools when every window slot is in the cache;
         otherwise pools the whole window (which fills the cache).
         state_ready: optional torch.cuda.Event (recorded after the absorb that
-        produced the state, on another stream) that the attention waits for."""
+        produced the state, on another stream) that the attention waits for.
+        after_pool_keys: the last kernel on `stream` is this layer's key pooling
+        (pool_slots), launched after Q and the state were written: the forward
+        may then start while it runs (HF_FWD_AFTER_POOL_KEYS)."""
         sm = self.slot_map()
         if self.rope is not None:
             self._forward_rope(Q, O, idx_out, stream, events, state_ready)
             return
         cached = all(sl in self.pooled for sl in sm)
         flags = (hb.HF_FWD_CACHED_KEYS if cached else 0) | self._state_flags()
+        if after_pool_keys:
+            flags |= hb.HF_FWD_AFTER_POOL_KEYS
         hb.hf_hybrid_forward_ex(self.cfg, Q, self.Kc, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O, idx_out,
                                 self.ws, flags, events, stream, state_ready)
         self.pooled.update(sm)
@@ -197,8 +202,8 @@ class HybridAttentionLayer:
                             r.base, stream)
         hb.hf_pool_keys(self.cfg, self.Kr, self.ss, sm, self.ws, stream)
         hb.hf_hybrid_forward_ex(self.cfg, self.Qr, self.Kr, self.Vc, self.ss, sm, self.n_win(), self.S, self.z, O,
-                                idx_out, self.ws, hb.HF_FWD_CACHED_KEYS | self._state_flags(), events, stream,
-                                state_ready)
+                                idx_out, self.ws, hb.HF_FWD_CACHED_KEYS | hb.HF_FWD_AFTER_POOL_KEYS | self._state_flags(),
+                                events, stream, state_ready)
         self.pooled.clear()   # the cache holds this step's rotated pools
         self.state_prepared = True
 
@@ -212,7 +217,7 @@ class HybridAttentionLayer:
         if not self.can_overlap_absorb():
             self.absorb_evicted(stream)
             self.write_chunk(K_new, V_new, stream)
-            self.forward(Q, O, idx_out, stream)
+            self.forward(Q, O, idx_out, stream, after_pool_keys=True)
             return
         # the absorb on a side stream; ring write, key pooling and the prologue
         # on `stream`; the attention (the only reader of the state) waits for it
@@ -225,7 +230,7 @@ class HybridAttentionLayer:
         self.absorb_evicted(self._side, share_sms=True)
         self._ev_state.record(self._side)
         self.write_chunk(K_new, V_new, main)
-        self.forward(Q, O, idx_out, main, state_ready=self._ev_state)
+        self.forward(Q, O, idx_out, main, state_ready=self._ev_state, after_pool_keys=True)
 
     # ---- checkpoint / resume ----
     def state_dict(self) -> dict:

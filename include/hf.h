@@ -259,12 +259,19 @@ HF_API hf_status hf_rope_relative(const hf_config *cfg, const uint16_t *src, uin
                                   or forward with this workspace (a fresh, zeroed
                                   workspace holds the operand of S = 0); the forward
                                   then does not read S (may be NULL) */
+#define HF_FWD_AFTER_POOL_KEYS 4u /* the last kernel launched on `stream` before
+                                  this call is hf_pool_keys, and every kernel that
+                                  wrote Q or S finished before that one started:
+                                  the forward's first kernel then starts while the
+                                  key pooling still runs (programmatic dependent
+                                  launch), reading Q and S meanwhile, and waits for
+                                  it only before it reads the pooled keys */
 
 /* Number of timing points of hf_hybrid_forward_ex / _profiled. */
 #define HF_FWD_EVENTS 4
 
 /* hf_hybrid_forward with options: `flags` (HF_FWD_CACHED_KEYS,
- * HF_FWD_STATE_PREPARED, or 0), per-kernel timing, `events` as in
+ * HF_FWD_STATE_PREPARED, HF_FWD_AFTER_POOL_KEYS, or 0), per-kernel timing, `events` as in
  * hf_hybrid_forward_profiled (may be NULL), and `state_ready` (a cudaEvent_t,
  * or NULL): the attention kernel, the only one that reads the state (its
  * operand and z), waits for it on `stream`, so the key pooling and the
