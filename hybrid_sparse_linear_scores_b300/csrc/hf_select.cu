@@ -791,16 +791,28 @@ __global__ void __launch_bounds__(256) fwd_prologue_kernel(const uint16_t* __res
 }
 
 // ---------------------------------------------------------------------------
-// Key pooling into the per-slot cache kpc [BH][W slots][D/4][bpf][4].  CTA = up to
-// 256 / beta consecutive blocks of one frame of one head (one bulk copy of
-// their rows out of the ring slot); the arithmetic is that of the prologue.
+// Key pooling into the per-slot cache kpc [BH][W slots][D/4][bpf][4].  CTA = one
+// key block of one frame of one head (one bulk copy of its rows out of the ring
+// slot, 128 threads); the arithmetic is that of the prologue.  Small CTAs, many
+// per SM: while some wait for their rows, others pool theirs.
 // ---------------------------------------------------------------------------
 template <int D, int BETA>
-__global__ void __launch_bounds__(256) pool_keys_kernel(const uint16_t* __restrict__ Kc, Geom g, PoolFrames pf,
+struct KeyPoolCfg {
+    static constexpr int NT = 128;
+    static constexpr int QG = 1;                        // key blocks per CTA
+    static constexpr int STAGE_BYTES = BETA * D * 2;    // the block's rows
+    static constexpr int OFF_QP = STAGE_BYTES;          // fp32 [D]: the pooled block
+    static constexpr int OFF_BAR = OFF_QP + D * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 16;
+    static constexpr int SMEM = OFF_MISC + 16;
+};
+
+template <int D, int BETA>
+__global__ void __launch_bounds__(128) pool_keys_kernel(const uint16_t* __restrict__ Kc, Geom g, PoolFrames pf,
                                                         float* __restrict__ kpc, uint32_t* status,
                                                         uint64_t wait_limit_ns)
 {
-    using Cfg = ProCfg<D, BETA>;
+    using Cfg = KeyPoolCfg<D, BETA>;
     constexpr int QG = Cfg::QG;
     extern __shared__ __align__(128) uint8_t smem[];
     // the forward prologue that follows may start now: it waits for this
@@ -957,7 +969,7 @@ template <int D, int BETA>
 static int launch_pool_keys_t(const uint16_t* Kc, const Geom& g, const PoolFrames& pf, float* kpc, uint32_t* status,
                               uint64_t wait_limit_ns, cudaStream_t st)
 {
-    using Cfg = ProCfg<D, BETA>;
+    using Cfg = KeyPoolCfg<D, BETA>;
     auto k = pool_keys_kernel<D, BETA>;
     cudaError_t e = set_smem(k, Cfg::SMEM);
     if (e != cudaSuccess) return (int)e;
