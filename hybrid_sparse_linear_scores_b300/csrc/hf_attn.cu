@@ -213,7 +213,7 @@ struct AttnParams {
     // Split mode (all three non-null): every CTA takes an equal share of the
     // rounds of all pairs; a pair cut between CTAs leaves a partial result per
     // part, and the part that finishes last merges them.
-    const int32_t* pair_rounds;   // [total_pairs] rounds of each pair's slab stream
+    const int32_t* pair_rounds;   // [total_pairs] weight of each pair's slab stream (round_weight units)
     float* partial;               // [grid][2 slots][2 tiles][d + 4 columns][128 rows]: O, m, l
     uint32_t* counters;           // [total_pairs][2] parts arrived per tile; zero between launches
 };
@@ -1426,8 +1426,8 @@ int launch_attn(const uint16_t* Q, const uint16_t* Kc, const uint16_t* Vc, const
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // split mode (fused forward with the score kernel's pair round counts): one
-    // CTA per SM, each an equal share of all pairs' rounds; otherwise whole pairs
+    // split mode (fused forward with the prologue's pair weights): one CTA per
+    // SM, each an equal share of all pairs' weighted rounds; otherwise whole pairs
     // in turn
     const bool split = fused && pair_rounds && partial && counters;
     p.pair_rounds = split ? pair_rounds : nullptr;

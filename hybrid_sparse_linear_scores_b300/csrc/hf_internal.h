@@ -76,7 +76,7 @@ struct WsLayout {
     size_t kp;       // fp32 [BH][W slots][d/4][bpf][4]: pooled keys of every ring slot (kept between calls)
     size_t smma;     // bf16 [BH][2][d*d]  (S hi / lo, MMA operand layout; kept between calls)
     size_t idx;      // int32 [BH][nQB][K_max] (the only region whose size follows topk)
-    size_t prounds;  // int32 [BH * pairs per head]: rounds of each tile pair's slab stream
+    size_t prounds;  // int32 [BH * pairs per head]: weight of each tile pair's slab stream
     size_t total_compact;   // end of the above: the attention runs without splitting pairs
     size_t partial;  // fp32 [kAttnMaxGrid][2][2][128][d + 4]: partial results of split pairs
     size_t total;
