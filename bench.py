@@ -624,6 +624,39 @@ def pinned_h2d_rate(dev, nbytes: int = 43130880, n: int = 10, trials: int = 3):
     return best
 
 
+def streamer_copies_alone(streamer, Qh, Kh, Vh, Oh, n: int):
+    """ms per chunk of the host streamer's own copies with no compute between
+    them: the same pinned buffers, the same calls (Q by one copy, K/V by the
+    ring write's pitched per-frame copies, O back on the device-to-host
+    stream once its chunk's copy-in has landed) on the same two copy streams.
+    Host wall clock over n chunks, as for the end-to-end figure; if the two
+    agree, the end-to-end step runs at the host link's rate."""
+    from hybrid_sparse_linear_scores_b300 import binding as hb
+    L = streamer.L
+    slots = L.chunk_slots()
+
+    def one(i):
+        b = i % 2
+        with torch.cuda.stream(streamer.h2d):
+            streamer.h2d.wait_event(streamer.ev_d2h[b])   # Qd[b] / Od[b] reuse, as the forward would
+            streamer.Qd[b].copy_(Qh, non_blocking=True)
+            hb.hf_ring_write(L.cfg, Kh, Vh, L.Kc, L.Vc, L.ss, slots, streamer.h2d)
+            streamer.ev_h2d[b].record(streamer.h2d)
+        with torch.cuda.stream(streamer.d2h):
+            streamer.d2h.wait_event(streamer.ev_h2d[b])
+            Oh[b].copy_(streamer.Od[b], non_blocking=True)
+            streamer.ev_d2h[b].record(streamer.d2h)
+
+    for i in range(4):
+        one(i)
+    streamer.synchronize()
+    t0 = time.perf_counter()
+    for i in range(n):
+        one(i)
+    streamer.synchronize()
+    return 1000 * (time.perf_counter() - t0) / n
+
+
 def run_hf(args):
     ws, rank, local = dist_env()
     dev = torch.device("cuda", local)
@@ -773,10 +806,13 @@ def run_hf(args):
         e2e_ms = max_over_ranks(1000 * (time.perf_counter() - t0) / n_e2e, ws, dev)
         L2.check_device_status()
         h2d_step = (streamer.h2d_bytes - b0) // n_e2e
+        copies_ms = streamer_copies_alone(streamer, Qh, Kh, Vh, Oh, n_e2e)
         e2e = {"value": job_throughput(fl["total"], ws, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_step,
                "d2h_bytes_per_step": (streamer.d2h_bytes - d0) // n_e2e, "ms_per_step": e2e_ms,
                "h2d_GB_s_implied": h2d_step / (e2e_ms * 1e-3) / 1e9,
+               "copies_alone_ms_per_step": copies_ms,
+               "h2d_GB_s_copies_alone": h2d_step / (copies_ms * 1e-3) / 1e9,
                "h2d_GB_s_plain_pinned_copy": pinned_h2d_rate(dev, int(h2d_step)),
                "how": "HostStreamer: per chunk, Q and the chunk's K/V copied from pinned host memory and O "
                       "copied back, on copy streams overlapped with the neighbouring chunks' compute; "
