@@ -1096,35 +1096,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float m_own = participated ? m_use : -INFINITY;
                         const float l_own = participated ? l_tot : 0.0f;
                         if (participated) tc_fence_after();
-                        {   // the whole row at once: one TMEM round trip
-                            uint32_t o[D / 32][32];
-                            if (participated) {
+                        // The head part of a pair (its round 0) ends its CTA's share, so it
+                        // usually runs after the other parts, which start the following
+                        // shares.  If they have all arrived, it is the last part: it merges
+                        // without writing its own partial result.
+                        bool all_in = false;
+                        if (me == c0) {
+                            if (r == 0) misc[M_OLD + t] = ld_acquire_gpu(p.counters + (size_t)pair * 2 + t);
+                            asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
+                            all_in = *reinterpret_cast<volatile uint32_t*>(&misc[M_OLD + t]) == (uint32_t)(nparts - 1);
+                        }
+                        if (!all_in) {
+                            {   // the whole row at once: one TMEM round trip
+                                uint32_t o[D / 32][32];
+                                if (participated) {
 #pragma unroll
-                                for (int cq = 0; cq < D / 32; ++cq) tmem_ld32_nw(o_col + 32 * cq, o[cq]);
-                                tmem_wait_ld();
+                                    for (int cq = 0; cq < D / 32; ++cq) tmem_ld32_nw(o_col + 32 * cq, o[cq]);
+                                    tmem_wait_ld();
 #pragma unroll
-                                for (int cq = 0; cq < D / 32; ++cq) reg_dep32(o[cq]);
-                            } else {
+                                    for (int cq = 0; cq < D / 32; ++cq) reg_dep32(o[cq]);
+                                } else {
+#pragma unroll
+                                    for (int cq = 0; cq < D / 32; ++cq)
+#pragma unroll
+                                        for (int c = 0; c < 32; ++c) o[cq][c] = 0u;
+                                }
 #pragma unroll
                                 for (int cq = 0; cq < D / 32; ++cq)
 #pragma unroll
-                                    for (int c = 0; c < 32; ++c) o[cq][c] = 0u;
+                                    for (int c = 0; c < 32; ++c)
+                                        __stcg(mine + (32 * cq + c) * 128, __uint_as_float(o[cq][c]));
                             }
-#pragma unroll
-                            for (int cq = 0; cq < D / 32; ++cq)
-#pragma unroll
-                                for (int c = 0; c < 32; ++c)
-                                    __stcg(mine + (32 * cq + c) * 128, __uint_as_float(o[cq][c]));
+                            __stcg(mine + D * 128, m_own);
+                            __stcg(mine + (D + 1) * 128, l_own);
+                            asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
+                            if (r == 0) {
+                                __threadfence();
+                                misc[M_OLD + t] = atomicAdd(p.counters + (size_t)pair * 2 + t, 1u);
+                            }
+                            asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
                         }
-                        __stcg(mine + D * 128, m_own);
-                        __stcg(mine + (D + 1) * 128, l_own);
-                        asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
-                        if (r == 0) {
-                            __threadfence();
-                            misc[M_OLD + t] = atomicAdd(p.counters + (size_t)pair * 2 + t, 1u);
-                        }
-                        asm volatile("bar.sync %0, 128;" ::"r"(2 + t) : "memory");
-                        do_out = *reinterpret_cast<volatile uint32_t*>(&misc[M_OLD + t]) == (uint32_t)(nparts - 1);
+                        do_out = all_in ||
+                                 *reinterpret_cast<volatile uint32_t*>(&misc[M_OLD + t]) == (uint32_t)(nparts - 1);
                         if (do_out && nparts == 2) {
                             // two parts (the usual cut): the other part's whole row is
                             // loaded at once (one memory round trip), then combined with

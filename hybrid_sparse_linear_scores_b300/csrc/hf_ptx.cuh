@@ -78,6 +78,16 @@ struct WaitCtl {
     uint64_t limit_ns;
 };
 
+// Load with acquire semantics at GPU scope: the writes another CTA made before
+// its release (a fence, then the atomic that published them) are visible to
+// this thread's later loads.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void report_error(const WaitCtl& w, uint32_t code, uint32_t site)
 {
     *w.abort_flag = 1;
