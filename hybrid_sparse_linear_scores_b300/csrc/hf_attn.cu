@@ -212,7 +212,7 @@ struct AttnParams {
     int spf;                // slabs per frame = ceil(nf / 64)
     // Split mode (all three non-null): every CTA takes an equal share of the
     // rounds of all pairs; a pair cut between CTAs leaves a partial result per
-    // part, and the part that finishes last merges them.
+    // part (but the last one to arrive), and the part that arrives last merges them.
     const int32_t* pair_rounds;   // [total_pairs] weight of each pair's slab stream (round_weight units)
     float* partial;               // [grid][2 slots][2 tiles][d + 4 columns][128 rows]: O, m, l
     uint32_t* counters;           // [total_pairs][2] parts arrived per tile; zero between launches
@@ -1067,8 +1067,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && participated)
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[B_O_DONE + t], 0, wc, SITE_ATTN_PV_DONE));
                 float l_tot = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
-                // ---- a pair cut between CTAs: every part leaves (O, m, l) of each row in
-                // its slot; the part that arrives last merges all parts in part order
+                // ---- a pair cut between CTAs: every part but the last to arrive leaves
+                // (O, m, l) of each row in its slot; the part that arrives last merges all
+                // parts in part order, its own from TMEM
                 // (so the result does not depend on which part that is) and finishes
                 // the pair ----
                 bool do_out = true;
