@@ -26,7 +26,7 @@ def hexf(h: str) -> float:
 
 
 def bf16(x) -> torch.Tensor:
-    return torch.as_tensor(np.asarray(x, np.float32)).to(torch.bfloat16)
+    return torch.as_tensor(np.array(x, np.float32)).to(torch.bfloat16)
 
 
 def rnd(shape, seed, scale=1.0):
