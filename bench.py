@@ -857,6 +857,8 @@ def run_hf(args):
                    "parallelism": f"replicas x{ws}"},
         "us_per_latent_frame": 1000 * ms / w.chunk_frames,
         "median_ms_per_step": statistics.median(step_ms),
+        "p10_ms_per_step": statistics.quantiles(step_ms, n=10)[0] if len(step_ms) > 1 else step_ms[0],
+        "p90_ms_per_step": statistics.quantiles(step_ms, n=10)[8] if len(step_ms) > 1 else step_ms[0],
         "median_us_per_latent_frame": 1000 * statistics.median(step_ms) / w.chunk_frames,
         "pct_bf16_peak": 100 * value / pk["bf16_tflops"],
         "warm_l2_ms_per_step": warm_ms,
