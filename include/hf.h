@@ -314,9 +314,9 @@ HF_API hf_status hf_hybrid_forward_profiled(const hf_config *cfg, const uint16_t
 /* The last HF_SPLIT_PARTIAL_BYTES(head_dim) bytes of hf_workspace_size() hold
  * the partial results of tile pairs that the attention kernel cuts between
  * CTAs to balance its work (every CTA takes an equal share of all pairs'
- * rounds, weighted by their MMA work).  A forward without them runs whole pairs per CTA instead: same
- * results up to rounding, less even work.  hf_hybrid_forward_noalloc runs
- * that way. */
+ * rounds, weighted by their MMA work).  A forward without them runs whole
+ * pairs per CTA instead: same results up to rounding, less even work.
+ * hf_hybrid_forward_noalloc runs that way. */
 #define HF_SPLIT_PARTIAL_BYTES(head_dim) (160u * 2u * 2u * 128u * ((unsigned)(head_dim) + 4u) * 4u)
 
 /* hf_hybrid_forward for callers that cannot allocate device memory.  The
